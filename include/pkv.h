@@ -1,0 +1,285 @@
+/*
+ * pkv.h -- C ABI of libpkv: a paged KV cache for one GPU (sm_103a).
+ *
+ * The method, as the pages on paged KV caches describe it:
+ *   "04 - Hacia PagedAttention (vista previa)", section "La idea de PagedAttention":
+ *     1. the KV cache is cut into fixed-size blocks of B_block tokens (B_block = 16);
+ *     2. every sequence keeps a block table: logical block i -> physical block X;
+ *     3. to extend a sequence by one token, write into its last block if it has room,
+ *        otherwise take a new physical block and extend the table;
+ *     4. freeing a sequence returns its blocks to a free list;
+ *     5. the attention kernel takes the block table as an argument and gathers internally.
+ *   "PagedAttention e continuous batching", section "01 - Conceito":
+ *     paragraph 3  blocks live anywhere in the pool; the allocator hands a sequence a new
+ *                  block when it outgrows its last one, without moving anything;
+ *     paragraph 6  identical prompt prefixes share read-only blocks; copy-on-write gives a
+ *                  diverging branch a new block; reference counts return blocks to the pool;
+ *     paragraph 7  admission reasons in countable blocks and refuses early, clearly;
+ *     paragraph 8  block metrics: free/used blocks, allocation failures, tail waste,
+ *                  prefix hits, preemptions.
+ *
+ * Two halves:
+ *   - device calls (kv append, paged decode attention, block copy): asynchronous on the
+ *     caller's CUDA stream, no host synchronisation, no allocation; every device pointer is
+ *     owned by the caller;
+ *   - a host block manager (pure C, no CUDA): free list, block tables, reference counts,
+ *     prefix sharing, copy-on-write decisions and admission in blocks.
+ *
+ * Memory layout (the pages fix none; this library's reading):
+ *   pool (K or V) = [n_layers][num_blocks][n_kv_heads][block_size][head_dim] elements,
+ *   row-major, so layer l starts at pool + l * num_blocks * n_kv_heads * block_size * head_dim
+ *   and one physical block id names the same 16 token positions in every layer (one block
+ *   table serves all layers, as the 1 MiB all-layer block of "01 - Conceito" paragraph 3).
+ *   slot of a token = physical block * block_size + (position mod block_size).
+ *   q, out   = [n_seqs][n_q_heads][head_dim]; query head h reads KV head h / (n_q / n_kv).
+ *   k, v     = [n_tokens][n_kv_heads][head_dim] (the new rows to append).
+ *   block_tables = int32 [n_seqs][max_blocks_per_seq]; context_lens = int32 [n_seqs].
+ *
+ * Status: every call returns PKV_OK (0) or one PKV_ERR_* code; pkv_status_str names it.
+ * Argument errors are caught on the host before anything is launched. Values that live on
+ * the device (table entries, context lengths, slots, copy pairs) are range-checked inside
+ * the kernels: a bad one is skipped and recorded in a device status word that
+ * pkv_get_device_status reads and clears; no kernel traps.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- types ------------------------------------------------------------------------- */
+
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, unknown id      */
+    PKV_ERR_UNSUPPORTED = 2, /* shape outside the compiled set (see pkv_cache_desc)        */
+    PKV_ERR_NO_BLOCKS = 3,   /* not enough free blocks: admission refused / append OOM      */
+    PKV_ERR_BAD_STATE = 4,   /* internal inconsistency detected (never expected)            */
+    PKV_ERR_CUDA = 5         /* a CUDA runtime call failed (launch, attribute, copy)         */
+};
+
+/* Device status bits, set by kernels that skipped a bad device-side value. */
+enum {
+    PKV_DEV_BAD_BLOCK_ID = 1u,    /* block table entry outside [0, num_blocks)               */
+    PKV_DEV_BAD_CONTEXT_LEN = 2u, /* context length < 0 or > max_blocks_per_seq*block_size  */
+    PKV_DEV_BAD_SLOT = 4u,        /* slot >= num_blocks*block_size                           */
+    PKV_DEV_BAD_PAIR = 8u,        /* copy pair id outside [0, num_blocks)                    */
+    PKV_DEV_WAIT_TIMEOUT = 16u    /* a bounded wait on an asynchronous copy gave up          */
+};
+
+/*
+ * Shape of one paged cache. Supported: block_size == 16; head_dim in {64, 128, 256};
+ * n_q_heads == G * n_kv_heads with G in {1, 2, 4, 8}; dtype in pkv_dtype; all counts >= 1.
+ * Anything else returns PKV_ERR_UNSUPPORTED (or PKV_ERR_INVALID_ARG for non-positive counts).
+ */
+typedef struct {
+    int32_t dtype;      /* pkv_dtype                                  */
+    int32_t n_layers;
+    int32_t num_blocks; /* physical blocks in the pool (every layer) */
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t block_size; /* tokens per block; must be 16               */
+} pkv_cache_desc;
+
+/* ---- descriptors and sizes --------------------------------------------------------- */
+
+const char* pkv_status_str(int status);
+
+/* PKV_OK if the descriptor is supported, else the error code the device calls would return. */
+int pkv_validate_desc(const pkv_cache_desc* desc);
+
+/*
+ * KV bytes one token occupies across all layers: 2 (K and V) * n_layers * n_kv_heads *
+ * head_dim * element bytes ("Paged Attention em Large Language Models LLMs", section
+ * "Configurando as Constantes": 524,288 bytes for 32 x 32 x 128 in fp16). 0 if desc is invalid.
+ */
+uint64_t pkv_bytes_per_token(const pkv_cache_desc* desc);
+
+/* Bytes of one pool (K or V) over all layers: n_layers*num_blocks*n_kv*block_size*head_dim*e. */
+uint64_t pkv_pool_bytes(const pkv_cache_desc* desc);
+
+/*
+ * Scratch bytes pkv_paged_decode_attention needs for n_seqs sequences whose tables have
+ * max_blocks_per_seq columns (split-K partial results; 0 when no split is needed).
+ */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq);
+
+/* ---- device calls ------------------------------------------------------------------ */
+
+/*
+ * Append the K/V rows of n_tokens new tokens of one layer into the pools
+ * ("La idea de PagedAttention", step 3; the slot comes from the block manager).
+ *   k, v          device, [n_tokens][n_kv_heads][head_dim] of desc->dtype, 16-byte aligned
+ *   slot_mapping  device int64 [n_tokens]; slot < 0 marks padding and is skipped;
+ *                 slot >= num_blocks*block_size is skipped and sets PKV_DEV_BAD_SLOT
+ *   k_pool, v_pool device, whole pools (all layers), 16-byte aligned
+ * Bit-exact byte copies. n_tokens == 0 is a no-op. Slots must be distinct (else the
+ * surviving row is unspecified).
+ */
+int pkv_kv_append(const pkv_cache_desc* desc, int32_t layer, const void* k, const void* v,
+                  const int64_t* slot_mapping, int32_t n_tokens, void* k_pool, void* v_pool,
+                  void* stream);
+
+/*
+ * Paged decode attention for one layer: one query token per sequence attends to the
+ * first context_lens[s] logical positions of its own cache, gathered through its block
+ * table ("La idea de PagedAttention", step 5). For query head h and KV head g = h / G:
+ *   out[s][h] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,  j < context_lens[s],
+ * K_j, V_j being row (block_tables[s][j / 16], g, j mod 16) of layer `layer`. Paging changes
+ * only where rows live, so this equals dense attention over the same rows ("Lo que deberias
+ * llevarte de la Fase 22 sobre la Fase 27", item 2). Accumulation is fp32; out is rounded
+ * to desc->dtype (round to nearest even). context_lens[s] == 0 gives a zero row.
+ *   q, out        device [n_seqs][n_q_heads][head_dim] of desc->dtype, 16-byte aligned
+ *   k_pool, v_pool device, whole pools (all layers), 16-byte aligned
+ *   block_tables  device int32 [n_seqs][max_blocks_per_seq]; only the first
+ *                 ceil(context_lens[s]/16) entries of row s are read
+ *   context_lens  device int32 [n_seqs], 0 <= len <= max_blocks_per_seq*16 (a larger one
+ *                 is clamped and sets PKV_DEV_BAD_CONTEXT_LEN)
+ *   workspace     device, >= pkv_decode_workspace_bytes(...) bytes, 16-byte aligned
+ *                 (may be NULL when that is 0); contents need no initialisation
+ * Rows outside the valid positions (tails of last blocks, unreferenced blocks) are never
+ * used: NaN there cannot reach the output. A table entry outside [0, num_blocks) is
+ * skipped (its rows count as masked) and sets PKV_DEV_BAD_BLOCK_ID.
+ */
+int pkv_paged_decode_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
+                               const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Copy-on-write block copies ("01 - Conceito", paragraph 6): for each pair (src, dst) in
+ * pairs (device int32 [n_pairs][2]) copy physical block src onto dst in K and V, all layers.
+ * Bit-exact. The dst ids must be distinct and disjoint from the src ids (else the result is
+ * unspecified). An id outside [0, num_blocks) skips its pair and sets PKV_DEV_BAD_PAIR.
+ */
+int pkv_copy_blocks(const pkv_cache_desc* desc, void* k_pool, void* v_pool, const int32_t* pairs,
+                    int32_t n_pairs, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear this library's device status word on the
+ * current device (PKV_DEV_* bits, 0 if every device-side value was in range). For tests
+ * and debugging; the only call here that blocks the host.
+ */
+int pkv_get_device_status(void* stream, uint32_t* flags);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t pkv_launch_count(void);
+
+/* ---- host block manager ------------------------------------------------------------ */
+
+typedef struct pkv_mgr pkv_mgr;
+
+typedef struct {
+    int64_t free_blocks;
+    int64_t used_blocks;
+    int64_t n_seqs;
+    int64_t alloc_failures;  /* refused admissions + appends that found no free block     */
+    int64_t tail_waste_rows; /* sum over sequences of 16*n_blocks - context length          */
+    int64_t prefix_hits;     /* blocks obtained by fork (shared) instead of allocation     */
+    int64_t cow_copies;      /* copy-on-write pairs emitted                                 */
+    int64_t append_oom;      /* appends refused for lack of blocks (a preemption signal)   */
+} pkv_stats;
+
+/*
+ * Create a manager over num_blocks physical blocks of block_size (16) tokens.
+ * initial_free_order (host, num_blocks ids, a permutation of 0..num_blocks-1) fixes the
+ * free list's initial order; NULL means 0, 1, ..., num_blocks-1. Returns NULL on bad
+ * arguments or allocation failure. The free list is FIFO: allocation takes the front,
+ * release appends to the back, a freed sequence releases its blocks in logical order.
+ */
+pkv_mgr* pkv_mgr_create(int32_t num_blocks, int32_t block_size, const int32_t* initial_free_order);
+
+/* Deep copy (checkpoint of the bookkeeping); NULL on allocation failure. */
+pkv_mgr* pkv_mgr_clone(const pkv_mgr* mgr);
+
+void pkv_mgr_destroy(pkv_mgr* mgr);
+
+/*
+ * Every manager call below is transactional: on any error the manager's state is unchanged
+ * (only the failure counters of pkv_stats move).
+ *
+ * Admit sequence seq_id with n_prompt_tokens tokens ("01 - Conceito", paragraph 7): it needs
+ * ceil(n_prompt/16) + ceil(reserve_tokens/16) free blocks, else PKV_ERR_NO_BLOCKS; only the
+ * prompt blocks are taken (reserve_tokens is headroom, not a reservation). slots_out (host,
+ * n_prompt_tokens entries, may be NULL) receives each prompt token's slot.
+ * PKV_ERR_INVALID_ARG if seq_id exists or a count is negative.
+ */
+int pkv_mgr_add_seq(pkv_mgr* mgr, int64_t seq_id, int32_t n_prompt_tokens, int32_t reserve_tokens,
+                    int64_t* slots_out);
+
+/*
+ * child starts as a copy of parent's table and context; every block gains a reference
+ * (prefix sharing, "01 - Conceito" paragraph 6). PKV_ERR_INVALID_ARG if parent is unknown,
+ * child exists, or they are equal.
+ */
+int pkv_mgr_fork(pkv_mgr* mgr, int64_t parent, int64_t child);
+
+/*
+ * Reserve the slot of one new token of seq_id ("La idea de PagedAttention", step 3):
+ *   last block full (or none): take a fresh block;
+ *   last block partially filled and referenced only by seq_id: write in place;
+ *   last block partially filled and shared: copy on write -- take a fresh block, report
+ *     (*cow_src, *cow_dst) for pkv_copy_blocks, drop one reference of the old block.
+ * *cow_src = *cow_dst = -1 when no copy is needed. PKV_ERR_NO_BLOCKS when a block is needed
+ * and none is free (counted in append_oom). Copy before append before attention.
+ */
+int pkv_mgr_append_slot(pkv_mgr* mgr, int64_t seq_id, int64_t* slot, int32_t* cow_src, int32_t* cow_dst);
+
+/*
+ * Append one token to each of seq_ids[0..n) in order. slots_out[n] receives the slots,
+ * cow_pairs_out[2*n] the (src, dst) pairs that were emitted, *n_cow their count, *n_done the
+ * number of sequences served. Stops at the first failing sequence and returns its status;
+ * the sequences before it stay appended (each single append is transactional).
+ */
+int pkv_mgr_append_batch(pkv_mgr* mgr, const int64_t* seq_ids, int32_t n, int64_t* slots_out,
+                         int32_t* cow_pairs_out, int32_t* n_cow, int32_t* n_done);
+
+/*
+ * Release seq_id ("La idea de PagedAttention", step 4): each block loses one reference and
+ * returns to the back of the free list when none is left. PKV_ERR_INVALID_ARG if unknown
+ * (double free).
+ */
+int pkv_mgr_free_seq(pkv_mgr* mgr, int64_t seq_id);
+
+/* Copy seq_id's table into out[cap]; *n_blocks and *ctx_len receive its size and length.
+ * PKV_ERR_INVALID_ARG if unknown or cap < n_blocks (nothing written then). */
+int pkv_mgr_block_table(const pkv_mgr* mgr, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_blocks,
+                        int32_t* ctx_len);
+
+/*
+ * Pack the tables of seq_ids[0..n) into tables_out[n][max_blocks] (unused entries = -1) and
+ * their lengths into lens_out[n]: the host image of the device arguments of
+ * pkv_paged_decode_attention. PKV_ERR_INVALID_ARG if an id is unknown or a table is wider
+ * than max_blocks.
+ */
+int pkv_mgr_pack_tables(const pkv_mgr* mgr, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
+                        int32_t* tables_out, int32_t* lens_out);
+
+int pkv_mgr_stats(const pkv_mgr* mgr, pkv_stats* out);
+
+/* Reference count of a block, or -1 if the id is out of range. */
+int32_t pkv_mgr_refcount(const pkv_mgr* mgr, int32_t block);
+
+/* Copy up to cap free-list entries, front first, into out; returns the free-list length. */
+int32_t pkv_mgr_free_list(const pkv_mgr* mgr, int32_t* out, int32_t cap);
+
+/*
+ * Fault injection for tests: the (after_n_allocs + 1)-th block allocation attempted from
+ * now on fails as if the pool were empty (once); a negative value disables it. Used to
+ * check that multi-block operations roll back completely.
+ */
+int pkv_mgr_inject_alloc_failure(pkv_mgr* mgr, int32_t after_n_allocs);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

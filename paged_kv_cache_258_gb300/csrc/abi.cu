@@ -1,0 +1,226 @@
+// abi.cu -- the C ABI of libpkv: argument validation, dispatch, device status word.
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+// Device status word: kernels OR PKV_DEV_* bits into it when they skip a bad device-side value.
+__device__ unsigned int g_dev_status;
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_status_mu;
+unsigned int* g_status_addr[64] = {};
+
+// Device address of this device's status word (resolved once per device).
+cudaError_t status_word(unsigned int** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_dev_status);
+        if (err != cudaSuccess) return err;
+        g_status_addr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_status_addr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+size_t layer_elems(const pkv_cache_desc* d) {
+    return (size_t)d->num_blocks * d->n_kv_heads * d->block_size * d->head_dim;
+}
+
+size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int* bpp_out, int* n_parts_out) {
+    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks);
+    const int n_parts = pkv::decode_partitions(max_blocks, bpp);
+    if (bpp_out) *bpp_out = bpp;
+    if (n_parts_out) *n_parts_out = n_parts;
+    if (n_parts <= 1) return 0;
+    return (size_t)n_seqs * d->n_q_heads * n_parts * (d->head_dim + 2) * sizeof(float);
+}
+
+}  // namespace
+
+namespace pkv {
+
+// Blocks per partition: 32 (512 tokens) unless the grid would then hold fewer than ~4 CTAs per
+// SM of a GB300 (152 SMs), in which case partitions shrink (down to 4 blocks) to spread one
+// long sequence over more SMs. Depends only on the arguments, so the workspace query and the
+// launch agree on every device.
+int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
+    const long long target = 4LL * 152;
+    int bpp = 32;
+    while (bpp > 4 && (long long)n_seqs * n_kv * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
+    return bpp;
+}
+
+cudaError_t launch_decode(int dtype, int head_dim, int group, const DecodeArgs& a, cudaStream_t stream,
+                          int* n_launches) {
+    switch (dtype) {
+    case PKV_F32: return launch_decode_f32(head_dim, group, a, stream, n_launches);
+    case PKV_F16: return launch_decode_f16(head_dim, group, a, stream, n_launches);
+    case PKV_BF16: return launch_decode_bf16(head_dim, group, a, stream, n_launches);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+const char* pkv_status_str(int status) {
+    switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG: invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape outside the compiled set";
+    case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS: not enough free blocks";
+    case PKV_ERR_BAD_STATE: return "PKV_ERR_BAD_STATE: internal inconsistency";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
+    default: return "unknown pkv status";
+    }
+}
+
+int pkv_validate_desc(const pkv_cache_desc* d) {
+    if (!d) return PKV_ERR_INVALID_ARG;
+    if (d->n_layers <= 0 || d->num_blocks <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 ||
+        d->block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (d->dtype != PKV_F32 && d->dtype != PKV_F16 && d->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (d->block_size != pkv::kBlock) return PKV_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return PKV_ERR_UNSUPPORTED;
+    if (d->n_q_heads % d->n_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+    const int G = d->n_q_heads / d->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+uint64_t pkv_bytes_per_token(const pkv_cache_desc* d) {
+    if (pkv_validate_desc(d) != PKV_OK) return 0;
+    return 2ull * (uint64_t)d->n_layers * (uint64_t)d->n_kv_heads * (uint64_t)d->head_dim * elem_bytes(d->dtype);
+}
+
+uint64_t pkv_pool_bytes(const pkv_cache_desc* d) {
+    if (pkv_validate_desc(d) != PKV_OK) return 0;
+    return (uint64_t)d->n_layers * layer_elems(d) * elem_bytes(d->dtype);
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* d, int32_t n_seqs, int32_t max_blocks_per_seq) {
+    if (pkv_validate_desc(d) != PKV_OK || n_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
+    return decode_workspace(d, n_seqs, max_blocks_per_seq, nullptr, nullptr);
+}
+
+int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const void* v, const int64_t* slot_mapping,
+                  int32_t n_tokens, void* k_pool, void* v_pool, void* stream) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (layer < 0 || layer >= d->n_layers || n_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (n_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+    pkv::AppendArgs a;
+    a.k = k;
+    a.v = v;
+    a.slots = slot_mapping;
+    const size_t layer_bytes = layer_elems(d) * elem_bytes(d->dtype);
+    a.k_layer = static_cast<char*>(k_pool) + (size_t)layer * layer_bytes;
+    a.v_layer = static_cast<char*>(v_pool) + (size_t)layer * layer_bytes;
+    a.n_tok = n_tokens;
+    a.n_kv = d->n_kv_heads;
+    a.num_blocks = d->num_blocks;
+    a.row_bytes = d->head_dim * (int)elem_bytes(d->dtype);
+    if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (layer < 0 || layer >= d->n_layers || n_seqs < 0) return PKV_ERR_INVALID_ARG;
+    if (n_seqs == 0) return PKV_OK;
+    if (max_blocks_per_seq <= 0 || max_blocks_per_seq > (1 << 24)) return PKV_ERR_INVALID_ARG;
+    if (n_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+    int bpp = 0, n_parts = 0;
+    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, &bpp, &n_parts);
+    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
+
+    pkv::DecodeArgs a;
+    const size_t layer_bytes = layer_elems(d) * elem_bytes(d->dtype);
+    a.q = q;
+    a.k_layer = static_cast<const char*>(k_pool) + (size_t)layer * layer_bytes;
+    a.v_layer = static_cast<const char*>(v_pool) + (size_t)layer * layer_bytes;
+    a.tables = block_tables;
+    a.lens = context_lens;
+    a.out = out;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = need ? a.part_o + (size_t)n_seqs * d->n_q_heads * n_parts * d->head_dim : nullptr;
+    a.n_seqs = n_seqs;
+    a.n_q = d->n_q_heads;
+    a.n_kv = d->n_kv_heads;
+    a.num_blocks = d->num_blocks;
+    a.max_blocks = max_blocks_per_seq;
+    a.n_parts = n_parts;
+    a.bpp = bpp;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
+    int launches = 0;
+    cudaError_t err = pkv::launch_decode(d->dtype, d->head_dim, d->n_q_heads / d->n_kv_heads, a,
+                                         static_cast<cudaStream_t>(stream), &launches);
+    g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,
+                    void* stream) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (n_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (n_pairs == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !pairs) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+    if (d->n_layers > 65535) return PKV_ERR_UNSUPPORTED;
+    pkv::CopyArgs a;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.pairs = pairs;
+    a.n_pairs = n_pairs;
+    a.n_layers = d->n_layers;
+    a.num_blocks = d->num_blocks;
+    a.block_bytes = (size_t)d->n_kv_heads * d->block_size * d->head_dim * elem_bytes(d->dtype);
+    a.layer_bytes = a.block_bytes * (size_t)d->num_blocks;
+    if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pkv::launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+int pkv_get_device_status(void* stream, uint32_t* flags) {
+    if (!flags) return PKV_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    unsigned int* addr = nullptr;
+    if (status_word(&addr) != cudaSuccess) return PKV_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, addr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemset(addr, 0, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+    *flags = v;
+    return PKV_OK;
+}
+
+uint64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,329 @@
+"""ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every compute step runs in the library's CUDA kernels; this module checks tensor placement,
+dtype, contiguity and shape, passes ``data_ptr()`` and the current CUDA stream, and turns
+status codes into exceptions. It never computes on the CPU and has no fallback: if
+libpkv.so is missing it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import numpy as np
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libpkv.so"
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_NO_BLOCKS, PKV_ERR_BAD_STATE, PKV_ERR_CUDA = range(6)
+STATUS_NAMES = {0: "ok", 1: "invalid", 2: "unsupported", 3: "no_blocks", 4: "bad_state", 5: "cuda"}
+PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT_LEN, PKV_DEV_BAD_SLOT, PKV_DEV_BAD_PAIR, PKV_DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+BLOCK = 16
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32)]
+
+    @property
+    def dtype_name(self) -> str:
+        return {v: k for k, v in DTYPE_CODES.items()}[self.dtype]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("free_blocks", "used_blocks", "n_seqs", "alloc_failures",
+                                              "tail_waste_rows", "prefix_hits", "cow_copies", "append_oom")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def lib():
+    """Load libpkv.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build() (needs nvcc)")
+    L = ctypes.CDLL(str(LIB_PATH))
+    c_i32, c_i64, c_u32, c_u64, c_sz, vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64,
+                                            ctypes.c_size_t, ctypes.c_void_p)
+    dp = ctypes.POINTER(CacheDesc)
+    i32p, i64p = ctypes.POINTER(c_i32), ctypes.POINTER(c_i64)
+    sigs = {
+        "pkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "pkv_validate_desc": (ctypes.c_int, [dp]),
+        "pkv_bytes_per_token": (c_u64, [dp]),
+        "pkv_pool_bytes": (c_u64, [dp]),
+        "pkv_decode_workspace_bytes": (c_sz, [dp, c_i32, c_i32]),
+        "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
+        "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
+                                                      vp, vp, c_sz, vp]),
+        "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
+        "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
+        "pkv_launch_count": (c_u64, []),
+        "pkv_mgr_create": (vp, [c_i32, c_i32, i32p]),
+        "pkv_mgr_clone": (vp, [vp]),
+        "pkv_mgr_destroy": (None, [vp]),
+        "pkv_mgr_add_seq": (ctypes.c_int, [vp, c_i64, c_i32, c_i32, i64p]),
+        "pkv_mgr_fork": (ctypes.c_int, [vp, c_i64, c_i64]),
+        "pkv_mgr_append_slot": (ctypes.c_int, [vp, c_i64, i64p, i32p, i32p]),
+        "pkv_mgr_append_batch": (ctypes.c_int, [vp, i64p, c_i32, i64p, i32p, i32p, i32p]),
+        "pkv_mgr_free_seq": (ctypes.c_int, [vp, c_i64]),
+        "pkv_mgr_block_table": (ctypes.c_int, [vp, c_i64, i32p, c_i32, i32p, i32p]),
+        "pkv_mgr_pack_tables": (ctypes.c_int, [vp, i64p, c_i32, c_i32, i32p, i32p]),
+        "pkv_mgr_stats": (ctypes.c_int, [vp, ctypes.POINTER(Stats)]),
+        "pkv_mgr_refcount": (c_i32, [vp, c_i32]),
+        "pkv_mgr_free_list": (c_i32, [vp, i32p, c_i32]),
+        "pkv_mgr_inject_alloc_failure": (ctypes.c_int, [vp, c_i32]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_str(status: int) -> str:
+    return lib().pkv_status_str(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != PKV_OK:
+        raise PkvError(rc, what)
+
+
+def make_desc(dtype: str, n_layers: int, num_blocks: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+              block_size: int = BLOCK) -> CacheDesc:
+    return CacheDesc(DTYPE_CODES[dtype], n_layers, num_blocks, n_q_heads, n_kv_heads, head_dim, block_size)
+
+
+# ---- torch marshalling --------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def torch_dtype(name: str):
+    t = _torch()
+    return {"f32": t.float32, "f16": t.float16, "bf16": t.bfloat16}[name]
+
+
+def _stream_handle(stream):
+    t = _torch()
+    if stream is None:
+        return ctypes.c_void_p(t.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(x, name, dtype=None, shape=None):
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(x.shape)}")
+    return ctypes.c_void_p(x.data_ptr())
+
+
+def pool_shape(desc: CacheDesc):
+    return (desc.n_layers, desc.num_blocks, desc.n_kv_heads, desc.block_size, desc.head_dim)
+
+
+def pkv_validate_desc(desc: CacheDesc) -> int:
+    return int(lib().pkv_validate_desc(ctypes.byref(desc)))
+
+
+def pkv_bytes_per_token(desc: CacheDesc) -> int:
+    return int(lib().pkv_bytes_per_token(ctypes.byref(desc)))
+
+
+def pkv_pool_bytes(desc: CacheDesc) -> int:
+    return int(lib().pkv_pool_bytes(ctypes.byref(desc)))
+
+
+def pkv_decode_workspace_bytes(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int) -> int:
+    return int(lib().pkv_decode_workspace_bytes(ctypes.byref(desc), int(n_seqs), int(max_blocks_per_seq)))
+
+
+def pkv_kv_append(desc: CacheDesc, layer: int, k, v, slot_mapping, k_pool, v_pool, stream=None) -> None:
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_tok = int(k.shape[0])
+    row = (n_tok, desc.n_kv_heads, desc.head_dim)
+    rc = lib().pkv_kv_append(
+        ctypes.byref(desc), int(layer), _dev(k, "k", dt, row), _dev(v, "v", dt, row),
+        _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,)), n_tok,
+        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        _stream_handle(stream))
+    _check(rc, "pkv_kv_append")
+
+
+def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, block_tables, context_lens,
+                               scale: float, out, workspace=None, stream=None) -> None:
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_seqs = int(q.shape[0])
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [n_seqs, max_blocks]")
+    max_blocks = int(block_tables.shape[1])
+    qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pkv_paged_decode_attention(
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
+        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(rc, "pkv_paged_decode_attention")
+
+
+def pkv_copy_blocks(desc: CacheDesc, k_pool, v_pool, pairs, stream=None) -> None:
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_pairs = int(pairs.shape[0])
+    rc = lib().pkv_copy_blocks(
+        ctypes.byref(desc), _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        _dev(pairs, "pairs", t.int32, (n_pairs, 2)), n_pairs, _stream_handle(stream))
+    _check(rc, "pkv_copy_blocks")
+
+
+def pkv_get_device_status(stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib().pkv_get_device_status(_stream_handle(stream), ctypes.byref(flags)), "pkv_get_device_status")
+    return int(flags.value)
+
+
+def pkv_launch_count() -> int:
+    return int(lib().pkv_launch_count())
+
+
+def alloc_workspace(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, device="cuda"):
+    """A device buffer of pkv_decode_workspace_bytes (allocated by torch; None when 0)."""
+    t = _torch()
+    n = pkv_decode_workspace_bytes(desc, n_seqs, max_blocks_per_seq)
+    return t.empty(max(n, 16) // 4 + 4, dtype=t.float32, device=device) if n else None
+
+
+# ---- host block manager -------------------------------------------------------------------------
+
+def _i64p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _i32p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+class BlockManager:
+    """Owner of one pkv_mgr handle; methods return the C status code (and outputs)."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK, free_order=None, _handle=None):
+        L = lib()
+        if _handle is not None:
+            self._h = _handle
+        else:
+            order = None
+            if free_order is not None:
+                order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+                if order.shape != (num_blocks,):
+                    raise ValueError("free_order must list every block once")
+            self._h = L.pkv_mgr_create(int(num_blocks), int(block_size), _i32p(order) if order is not None else None)
+        if not self._h:
+            raise PkvError(PKV_ERR_INVALID_ARG, "pkv_mgr_create")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.pkv_mgr_destroy(h)
+            self._h = None
+
+    def clone(self) -> "BlockManager":
+        h = lib().pkv_mgr_clone(self._h)
+        if not h:
+            raise PkvError(PKV_ERR_BAD_STATE, "pkv_mgr_clone")
+        return BlockManager(self.num_blocks, self.block_size, _handle=h)
+
+    def add_seq(self, seq_id: int, n_prompt: int, reserve_tokens: int = 0):
+        slots = np.zeros(max(int(n_prompt), 1), dtype=np.int64)
+        rc = lib().pkv_mgr_add_seq(self._h, int(seq_id), int(n_prompt), int(reserve_tokens), _i64p(slots))
+        return rc, (slots[:n_prompt] if rc == PKV_OK else slots[:0])
+
+    def fork(self, parent: int, child: int) -> int:
+        return lib().pkv_mgr_fork(self._h, int(parent), int(child))
+
+    def append_slot(self, seq_id: int):
+        slot, src, dst = ctypes.c_int64(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)
+        rc = lib().pkv_mgr_append_slot(self._h, int(seq_id), ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst))
+        return rc, int(slot.value), int(src.value), int(dst.value)
+
+    def append_batch(self, seq_ids):
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = len(ids)
+        slots = np.zeros(max(n, 1), dtype=np.int64)
+        pairs = np.zeros(max(2 * n, 2), dtype=np.int32)
+        n_cow, n_done = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = lib().pkv_mgr_append_batch(self._h, _i64p(ids), n, _i64p(slots), _i32p(pairs),
+                                        ctypes.byref(n_cow), ctypes.byref(n_done))
+        return rc, slots[:n_done.value], pairs[:2 * n_cow.value].reshape(-1, 2), int(n_done.value)
+
+    def free_seq(self, seq_id: int) -> int:
+        return lib().pkv_mgr_free_seq(self._h, int(seq_id))
+
+    def block_table(self, seq_id: int):
+        nb, ctx = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = lib().pkv_mgr_block_table(self._h, int(seq_id), None, 0, ctypes.byref(nb), ctypes.byref(ctx))
+        if rc != PKV_OK and nb.value == 0 and ctx.value == 0:
+            return rc, [], 0
+        buf = np.zeros(max(nb.value, 1), dtype=np.int32)
+        rc = lib().pkv_mgr_block_table(self._h, int(seq_id), _i32p(buf), nb.value, ctypes.byref(nb), ctypes.byref(ctx))
+        return rc, buf[:nb.value].tolist(), int(ctx.value)
+
+    def pack_tables(self, seq_ids, max_blocks: int, tables_out=None, lens_out=None):
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = len(ids)
+        tables = tables_out if tables_out is not None else np.empty((n, max_blocks), dtype=np.int32)
+        lens = lens_out if lens_out is not None else np.empty(n, dtype=np.int32)
+        rc = lib().pkv_mgr_pack_tables(self._h, _i64p(ids), n, int(max_blocks), _i32p(tables), _i32p(lens))
+        return rc, tables, lens
+
+    def stats(self) -> dict:
+        st = Stats()
+        _check(lib().pkv_mgr_stats(self._h, ctypes.byref(st)), "pkv_mgr_stats")
+        return st.as_dict()
+
+    def refcount(self, block: int) -> int:
+        return int(lib().pkv_mgr_refcount(self._h, int(block)))
+
+    def refcounts(self):
+        return [self.refcount(b) for b in range(self.num_blocks)]
+
+    def free_list(self):
+        buf = np.zeros(max(self.num_blocks, 1), dtype=np.int32)
+        n = lib().pkv_mgr_free_list(self._h, _i32p(buf), self.num_blocks)
+        return buf[:n].tolist()
+
+    def inject_alloc_failure(self, after_n_allocs: int) -> int:
+        return lib().pkv_mgr_inject_alloc_failure(self._h, int(after_n_allocs))

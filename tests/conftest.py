@@ -13,6 +13,15 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 
 
+def pytest_sessionstart(session):
+    # libpkv.so and the oracle are rebuilt only when their sources changed (stamped).
+    from paged_kv_cache_258_gb300 import build as pkv_build
+    import oracle
+
+    pkv_build.build()
+    oracle.build()
+
+
 def gpu_available() -> bool:
     try:
         import torch

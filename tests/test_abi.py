@@ -1,0 +1,96 @@
+"""The C ABI library loads and exports every symbol include/pkv.h declares; host-only calls.
+
+No compute call here: device entry points are only checked for their host-side argument
+validation paths that return before any CUDA call.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from paged_kv_cache_258_gb300 import pkv
+
+HEADERS = sorted((Path(__file__).resolve().parent.parent / "include").glob("*.h"))
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(pkv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 20
+    L = pkv.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # the binding declares a signature for exactly the functions the header declares
+    import inspect
+    src = inspect.getsource(pkv.lib)
+    bound = set(re.findall(r'"(pkv_\w+)":', src))
+    assert bound == set(names)
+
+
+def test_bytes_per_token_matches_pages(golden):
+    g = golden["kv_bytes_per_token_gpt"]
+    d = pkv.make_desc("f16", g["n_layers"], 100, 32, g["n_kv_heads"], g["head_dim"])
+    assert pkv.pkv_bytes_per_token(d) == g["value"]
+    d = pkv.make_desc("bf16", 16, 100, 16, 4, 256)
+    assert pkv.pkv_bytes_per_token(d) * 16 == golden["longdoc_block_bytes"]["value"]
+    assert pkv.pkv_pool_bytes(d) == 16 * 100 * 4 * 16 * 256 * 2
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dtype="f16", n_layers=1, num_blocks=8, n_q_heads=8, n_kv_heads=2, head_dim=128), pkv.PKV_OK),
+    (dict(dtype="f32", n_layers=1, num_blocks=8, n_q_heads=16, n_kv_heads=2, head_dim=64), pkv.PKV_OK),
+    (dict(dtype="bf16", n_layers=1, num_blocks=8, n_q_heads=6, n_kv_heads=2, head_dim=128), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(dtype="f16", n_layers=1, num_blocks=8, n_q_heads=32, n_kv_heads=2, head_dim=128), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(dtype="f16", n_layers=1, num_blocks=8, n_q_heads=2, n_kv_heads=2, head_dim=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(dtype="f16", n_layers=0, num_blocks=8, n_q_heads=2, n_kv_heads=2, head_dim=64), pkv.PKV_ERR_INVALID_ARG),
+    (dict(dtype="f16", n_layers=1, num_blocks=8, n_q_heads=2, n_kv_heads=2, head_dim=64, block_size=32),
+     pkv.PKV_ERR_UNSUPPORTED),
+])
+def test_validate_desc(kw, want):
+    assert pkv.pkv_validate_desc(pkv.make_desc(**kw)) == want
+
+
+def test_workspace_only_when_split():
+    d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)
+    assert pkv.pkv_decode_workspace_bytes(d, 64, 32) == 0          # one partition per sequence
+    n = pkv.pkv_decode_workspace_bytes(d, 64, 129)                 # 129 blocks -> 5 partitions of 32
+    assert n == 64 * 32 * 5 * (128 + 2) * 4
+    d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)
+    assert pkv.pkv_decode_workspace_bytes(d4, 10, 2048) == 10 * 16 * 64 * (256 + 2) * 4
+    assert pkv.pkv_decode_workspace_bytes(d, 0, 10) == 0
+
+
+def test_device_calls_reject_bad_arguments_before_launch():
+    L = pkv.lib()
+    d = pkv.make_desc("f16", 2, 16, 4, 4, 64)
+    bad = pkv.make_desc("f16", 2, 16, 4, 3, 64)
+    null = ctypes.c_void_p(0)
+    assert L.pkv_kv_append(ctypes.byref(bad), 0, null, null, null, 1, null, null, null) == pkv.PKV_ERR_UNSUPPORTED
+    assert L.pkv_kv_append(ctypes.byref(d), 2, null, null, null, 1, null, null, null) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_kv_append(ctypes.byref(d), 0, null, null, null, 0, null, null, null) == pkv.PKV_OK
+    assert L.pkv_kv_append(ctypes.byref(d), 0, null, null, null, 3, null, null, null) == pkv.PKV_ERR_INVALID_ARG
+    mis = ctypes.c_void_p(0x1008)
+    assert L.pkv_kv_append(ctypes.byref(d), 0, mis, mis, mis, 3, mis, mis, null) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_paged_decode_attention(ctypes.byref(d), 0, null, null, null, null, 4, null, 0, 1.0, null, null, 0,
+                                        null) == pkv.PKV_OK
+    assert L.pkv_paged_decode_attention(ctypes.byref(d), 0, null, null, null, null, 4, null, 3, 1.0, null, null, 0,
+                                        null) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_copy_blocks(ctypes.byref(d), null, null, null, 0, null) == pkv.PKV_OK
+    assert L.pkv_copy_blocks(ctypes.byref(d), null, null, null, -1, null) == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.status_str(pkv.PKV_ERR_NO_BLOCKS).startswith("PKV_ERR_NO_BLOCKS")
+
+
+def test_manager_create_rejects_non_permutation():
+    L = pkv.lib()
+    import numpy as np
+    bad = np.array([0, 1, 1], dtype=np.int32)
+    assert not L.pkv_mgr_create(3, 16, bad.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    assert not L.pkv_mgr_create(0, 16, None)
