@@ -1,0 +1,537 @@
+"""Benchmark: paged decode attention on one GB300 (KV GB/s, decode tokens/s, % of HBM roofline).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gpt|ragged|longdoc|prefix]
+                    [--impl pkv|reference]
+
+A step is one decode step of the whole hot path over one batch: the host block manager
+reserves a slot per sequence (copy-on-write pairs included), the metadata goes to the device,
+then copy_blocks, and per layer kv_append + paged decode attention. ``value`` is the KV bytes
+the attention read per step (sum of context lengths x 2 x n_kv x head_dim x bytes x layers)
+divided by the step time, with the step's inputs already in HBM; ``e2e`` is the same metric
+with the per-step inputs (q, new K/V rows for every layer) copied from pinned host memory and
+the outputs copied back inside the timed region.
+
+Every input is synthetic and seeded (see paged_kv_cache_258_gb300/workloads.py). Multi-GPU
+(torchrun) runs one independent replica per rank (weak scaling: sequences shard across ranks
+with no data-path collective); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+from paged_kv_cache_258_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s & tokens/s at 1 GB300; % of HBM roofline"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed helpers (host logic; tested with gloo ranks on the CPU)
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_over_ranks(x: float, op: str, device=None) -> float:
+    """max or sum of a float over ranks (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.15)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, pw, reasons = [], [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+                pw.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device_index)
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text())
+        except ValueError:
+            pass
+    return {}
+
+
+# ---------------------------------------------------------------------------------------------
+# workloads
+
+def build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
+    """(workload, initial prompt per sequence, churn log or None)."""
+    extra = warmup + 2 * steps + 2 * W.BLOCK
+    if name == "gpt":
+        wl = W.gpt(seed=W.BASE_SEED + 1 + seed_offset, extra_tokens_per_seq=extra)
+        desc = "gpt: 32 layers x 32 heads x head_dim 128 fp16 (512 KiB/token), batch 64, block 16, " \
+               "ctx = min(U{64..512} + Geom(1/500), 2048)"
+    elif name == "ragged":
+        wl = W.ragged(seed=W.BASE_SEED + 2 + seed_offset, extra_tokens_per_seq=extra)
+        desc = "ragged: 1 layer, 32 heads x head_dim 128 fp16, 32 sequences, ctx log-uniform [5, 8192] incl. " \
+               "60/200/1500, block 16, shuffled free list"
+    elif name == "longdoc":
+        wl = W.longdoc(seed=W.BASE_SEED + 3 + seed_offset, extra_tokens_per_seq=extra)
+        desc = "longdoc: 16 layers, GQA 16 q / 4 kv heads x head_dim 256 bf16 (64 KiB/token), " \
+               "10 sequences x 32,768 tokens, block 16, split-K"
+    elif name == "prefix":
+        churn = W.prefix_churn(seed=W.BASE_SEED + 4 + seed_offset)
+        wl = W.Workload("prefix", "f16", 1, 32, 32, 128, np.zeros(200, dtype=np.int32), churn.num_blocks,
+                        churn.seed)
+        desc = "prefix: 1 layer, 32 heads x head_dim 128 fp16, 200 sequences forked from 8 roots sharing a " \
+               "1024+t token prompt, 1 token/sequence/step, 5% replaced per step, CoW on first divergent write"
+        return wl, desc, churn
+    else:
+        raise ValueError(name)
+    return wl, desc, None
+
+
+def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int = 0):
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+    from paged_kv_cache_258_gb300.engine import DecodeBatch, PagedKVCache
+
+    wl, wdesc, churn = build_workload(name, warmup, steps, seed_offset)
+    desc = pkv.make_desc(wl.dtype, wl.n_layers, wl.num_blocks, wl.n_q_heads, wl.n_kv_heads, wl.head_dim)
+    cache = PagedKVCache(desc, free_order=W.free_order(wl.num_blocks, wl.seed), device=device, init="randn",
+                         seed=wl.seed)
+    extra = warmup + 2 * steps + 2 * W.BLOCK
+    if churn is None:
+        for s, n in enumerate(wl.context_lens):
+            cache.add_sequence(s, int(n) - 1)   # the first step appends the token that makes ctx
+        ids = list(range(wl.n_seqs))
+        max_blocks = int(-(-(int(wl.context_lens.max()) + extra) // W.BLOCK))
+    else:
+        roots = [10 ** 6 + g for g in range(churn.n_groups)]
+        for g, r in enumerate(roots):
+            cache.add_sequence(r, churn.group_prompt[g])
+        for m, g in enumerate(churn.member_group):
+            cache.fork(roots[churn.member_group[m]], m)
+        ids = list(range(len(churn.member_group)))
+        max_blocks = int(-(-(max(churn.group_prompt) + extra) // W.BLOCK))
+    batch = DecodeBatch(cache, ids, max_blocks)
+    n = len(ids)
+    dt = pkv.torch_dtype(wl.dtype)
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed + 7)
+    L = wl.n_layers
+    q = torch.randn((L, n, wl.n_q_heads, wl.head_dim), dtype=dt, device=device, generator=g)
+    k_new = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), dtype=dt, device=device, generator=g)
+    v_new = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), dtype=dt, device=device, generator=g)
+    out = torch.empty_like(q)
+    state = {"churn": churn, "step": 0, "live": list(ids), "roots": [10 ** 6 + i for i in range(8)]}
+    return wl, wdesc, cache, batch, (q, k_new, v_new, out), state
+
+
+def apply_churn(cache, batch, state):
+    churn = state["churn"]
+    if churn is None or state["step"] >= len(churn.steps):
+        state["step"] += 1
+        return
+    live = state["live"]
+    for old, new, g in churn.steps[state["step"]]:
+        cache.free(old)
+        cache.fork(state["roots"][g], new)
+        live[live.index(old)] = new
+    batch.set_sequences(live)
+    state["step"] += 1
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+
+def run_gpu(args) -> dict | None:
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pkv.lib()
+    wl, wdesc, cache, batch, (q, k_new, v_new, out), state = setup_gpu_case(
+        args.config, args.warmup, args.steps, device, seed_offset=rank)
+    stream = batch.stream
+    scale = wl.scale
+
+    for _ in range(args.warmup):
+        batch.step(q, k_new, v_new, out, scale)
+        apply_churn(cache, batch, state)
+    flags = pkv.pkv_get_device_status(stream)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} during warm-up")
+
+    # ---- timed region: inputs resident in HBM ----
+    L = wl.n_layers
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps * L)]
+    layer_bytes = []
+    cursor = {"i": 0}
+
+    def on_decode(layer, when):
+        e = ev_pairs[cursor["i"]]
+        if when == "start":
+            e[0].record(stream)
+        else:
+            e[1].record(stream)
+            cursor["i"] += 1
+
+    sampler = ClockSampler(gpu_uuid(local))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.pkv_launch_count()
+    kv_bytes = 0
+    cow_pairs = 0
+    host_plan_s = 0.0
+    t0.record(stream)
+    for _ in range(args.steps):
+        h0 = time.perf_counter()
+        st = batch.plan()
+        host_plan_s += time.perf_counter() - h0
+        batch.upload(st)
+        batch.run_device(st, q, k_new, v_new, out, scale, on_decode)
+        b = batch.kv_bytes_last_step()
+        kv_bytes += b
+        layer_bytes.extend([b // L] * L)
+        cow_pairs += st["npairs"]
+        apply_churn(cache, batch, state)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = pkv.pkv_launch_count() - launches0
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = reduce_over_ranks(elapsed_ms, "max", device)
+    total_bytes = reduce_over_ranks(kv_bytes, "sum", device)
+    total_seqs = reduce_over_ranks(batch.n * args.steps, "sum", device)
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError("device status flags set during the timed region")
+
+    durs = [a.elapsed_time(b) for a, b in ev_pairs]
+    achieved_gbs = sum(layer_bytes) / (sum(durs) * 1e-3) / 1e9
+
+    # ---- e2e: per-step inputs from pinned host memory, outputs back to pinned host memory ----
+    e2e = run_e2e(args, batch, cache, state, (q, k_new, v_new, out), scale, device)
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) K/V/q; shapes and length mixes of the pages' workloads)",
+        "config": {
+            "workload": wdesc,
+            "kv_dtype": wl.dtype,
+            "n_seqs_per_gpu": batch.n,
+            "layers": L,
+            "q_heads": wl.n_q_heads,
+            "kv_heads": wl.n_kv_heads,
+            "head_dim": wl.head_dim,
+            "block_size": W.BLOCK,
+            "kv_gib_per_step": round(kv_bytes / args.steps / 2 ** 30, 3),
+            "l2": "no flush: every step reads more KV than the 129 MB L2 holds",
+            "parallelism": f"replicas x{ws} (sequences shard by rank, no collective)",
+        },
+        "tokens_per_s": round(total_seqs / (elapsed_ms * 1e-3), 1),
+        "hbm_frac_of_measured": round(value / hbm_peak, 4),
+        "hbm_frac_of_nominal_7900": round(value / NOMINAL_HBM_GBS, 4),
+        "roofline": {
+            "kernel": "paged_decode_kernel (+ splitk_combine_kernel when a sequence has several partitions)",
+            "bound": "hbm",
+            "achieved": round(achieved_gbs, 2),
+            "peak": hbm_peak,
+            "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
+            "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm_peak, 4),
+            "traffic": traffic_per_launch(args.config, sum(layer_bytes) / len(layer_bytes)),
+            "launch_ms_mean": round(sum(durs) / len(durs), 5),
+            "algorithmic_bytes_per_launch": int(sum(layer_bytes) / len(layer_bytes)),
+        },
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "host_plan_us_per_step": round(host_plan_s / args.steps * 1e6, 1),
+        "cow_pairs_timed": int(cow_pairs),
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cache, batch, wl, budget_s=args.cpu_budget)
+    return line
+
+
+def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
+    import torch
+    q, k_new, v_new, out = bufs
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k_new, v_new))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = batch.stream
+    meta = batch.n * 8 + batch.n * batch.max_blocks * 4 + batch.n * 4
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + meta
+    d2h = hout.numel() * hout.element_size()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    kv = 0
+    npairs = 0
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            q.copy_(hq, non_blocking=True)
+            k_new.copy_(hk, non_blocking=True)
+            v_new.copy_(hv, non_blocking=True)
+            st = batch.step(q, k_new, v_new, out, scale)
+            hout.copy_(out, non_blocking=True)
+            kv += batch.kv_bytes_last_step()
+            npairs += st["npairs"]
+            apply_churn(cache, batch, state)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
+    kv = reduce_over_ranks(kv, "sum", device)
+    return {"value": round(kv / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d + 8 * npairs // max(args.steps, 1)), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / args.steps, 4)}
+
+
+def traffic_per_launch(config: str, algorithmic: float):
+    """DRAM bytes per decode launch from the committed ncu capture, if it matches this kernel."""
+    f = ROOT / "profiles" / f"paged_decode_{config}.traffic.json"
+    if not f.exists():
+        return None
+    try:
+        rec = json.loads(f.read_text())
+    except ValueError:
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None  # the kernel changed since the counters were taken
+    ratio = rec.get("dram_bytes_per_algorithmic_byte")
+    return None if ratio is None else int(ratio * algorithmic)
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = ROOT / "paged_kv_cache_258_gb300" / "csrc"
+    for name in ("decode.cuh", "common.cuh", "internal.h"):
+        h.update((csrc / name).read_bytes())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle (reported baseline, and the reference arm)
+
+def _host_pool(t, dtype: str) -> np.ndarray:
+    import torch
+    if dtype == "bf16":
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def cpu_baseline(cache, batch, wl, budget_s: float = 12.0) -> dict:
+    """The fp64 oracle, as it stands, on this host's cores over whole layers of the same batch."""
+    import oracle
+    threads = os.cpu_count() or 1
+    st = batch._stage[batch._turn ^ 1]
+    tables = st["tables"].numpy().copy()
+    lens = st["lens"].numpy().copy()
+    dtype = wl.dtype
+    q_all = None
+    done_bytes, elapsed, layers = 0, 0.0, 0
+    per_layer = int(lens.astype(np.int64).sum()) * cache.kv_bytes_per_token_layer()
+    rng = np.random.default_rng(wl.seed + 11)
+    for layer in range(wl.n_layers):
+        kp = _host_pool(cache.k_pool[layer], dtype)
+        vp = _host_pool(cache.v_pool[layer], dtype)
+        q_all = W.normal_values(rng, (batch.n, wl.n_q_heads, wl.head_dim), dtype)
+        t0 = time.perf_counter()
+        oracle.paged_decode(dtype, q_all, kp, vp, tables, lens, wl.scale, n_threads=threads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += per_layer
+        layers += 1
+        if elapsed >= budget_s:
+            break
+    return {"value": round(done_bytes / elapsed / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{layers} of {wl.n_layers} layers x all {batch.n} sequences x {wl.n_q_heads} heads "
+                      f"(fp64 C oracle, OpenMP over (sequence, head)); {elapsed:.1f} s",
+            "tokens_per_s": round(batch.n * layers / wl.n_layers / elapsed, 3)}
+
+
+def run_reference(args) -> dict | None:
+    """The reference arm: the fp64 CPU oracle timed on this host's cores, same config and metric."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl, wdesc, churn = build_workload(args.config, args.warmup, args.steps)
+    rng = np.random.default_rng(wl.seed)
+    threads = os.cpu_count() or 1
+    if churn is not None:
+        lens = np.array([churn.group_prompt[g] + 1 for g in churn.member_group], dtype=np.int32)
+    else:
+        lens = wl.context_lens.copy()
+    # one layer's worth of the workload, sequences taken in order until the sample is ~0.3 s of work
+    n_take = len(lens)
+    if args.config == "longdoc":
+        n_take = 1
+    elif args.config in ("gpt", "prefix"):
+        n_take = 16 if args.config == "gpt" else 32
+    sel = lens[:n_take]
+    nb = int(np.sum(-(-sel.astype(np.int64) // W.BLOCK)))
+    tables = W.shuffled_tables(sel, nb, wl.seed)
+    kp = W.normal_values(rng, (nb, wl.n_kv_heads, W.BLOCK, wl.head_dim), wl.dtype)
+    vp = W.normal_values(rng, (nb, wl.n_kv_heads, W.BLOCK, wl.head_dim), wl.dtype)
+    q = W.normal_values(rng, (n_take, wl.n_q_heads, wl.head_dim), wl.dtype)
+    step_bytes = int(sel.astype(np.int64).sum()) * 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+    for _ in range(args.warmup):
+        oracle.paged_decode(wl.dtype, q, kp, vp, tables, sel, wl.scale, n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_decode(wl.dtype, q, kp, vp, tables, sel, wl.scale, n_threads=threads)
+    el = time.perf_counter() - t0
+    value = step_bytes * args.steps / el / 1e9
+    sample = f"per step: 1 layer x {n_take} of {wl.n_seqs if churn is None else len(lens)} sequences x " \
+             f"{wl.n_q_heads} heads (fp64 C oracle, {threads} threads)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": wdesc, "kv_dtype": wl.dtype},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="gpt", choices=["gpt", "ragged", "longdoc", "prefix"])
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+"""A paged KV cache on one GPU and its decode step, on top of the C ABI.
+
+``PagedKVCache`` owns the all-layer K/V pools (torch device memory) and the host C block
+manager. ``DecodeBatch`` runs decode steps for a fixed list of sequences in the order the
+method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAttention", steps
+3 and 5; "PagedAttention e continuous batching", "01 - Conceito", paragraph 6):
+
+  1. host:   the block manager reserves one slot per sequence (taking a fresh block or
+             copying a shared tail on write) and packs the block tables;
+  2. H2D:    slots, tables, lengths and copy pairs go to device buffers (pinned staging,
+             double-buffered so the host can plan step i+1 while step i's copy is pending);
+  3. device: copy-on-write block copies, then per layer the KV append and the paged decode
+             attention -- copies before appends (else a copy would overwrite the new row),
+             appends before attention (the new token attends to itself).
+
+All device work is in libpkv's kernels; this module only moves arguments.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import pkv
+
+
+class PagedKVCache:
+    def __init__(self, desc: pkv.CacheDesc, free_order=None, device=None, init: str = "zeros", seed: int = 0):
+        import torch
+        self.desc = desc
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        dt = pkv.torch_dtype(desc.dtype_name)
+        shape = pkv.pool_shape(desc)
+        if init == "randn":
+            g = torch.Generator(device=self.device)
+            g.manual_seed(seed)
+            self.k_pool = torch.randn(shape, dtype=dt, device=self.device, generator=g)
+            self.v_pool = torch.randn(shape, dtype=dt, device=self.device, generator=g)
+        else:
+            self.k_pool = torch.zeros(shape, dtype=dt, device=self.device)
+            self.v_pool = torch.zeros(shape, dtype=dt, device=self.device)
+        self.mgr = pkv.BlockManager(desc.num_blocks, desc.block_size, free_order=free_order)
+
+    def add_sequence(self, seq_id: int, n_prompt: int, reserve_tokens: int = 0) -> np.ndarray:
+        rc, slots = self.mgr.add_seq(seq_id, n_prompt, reserve_tokens)
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, f"add_seq({seq_id}, {n_prompt})")
+        return slots
+
+    def fork(self, parent: int, child: int) -> None:
+        rc = self.mgr.fork(parent, child)
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, f"fork({parent}, {child})")
+
+    def free(self, seq_id: int) -> None:
+        rc = self.mgr.free_seq(seq_id)
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, f"free_seq({seq_id})")
+
+    def kv_bytes_per_token_layer(self) -> int:
+        d = self.desc
+        return 2 * d.n_kv_heads * d.head_dim * (4 if d.dtype_name == "f32" else 2)
+
+
+class DecodeBatch:
+    """Decode steps for a batch of n sequences whose tables are at most max_blocks wide."""
+
+    def __init__(self, cache: PagedKVCache, seq_ids, max_blocks: int, stream=None):
+        import torch
+        self.cache = cache
+        self.seq_ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        self.n = len(self.seq_ids)
+        self.max_blocks = int(max_blocks)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
+        dev = cache.device
+        n, mb = self.n, self.max_blocks
+        # device metadata (fixed addresses: the launches see the same pointers every step)
+        self.d_slots = torch.empty(n, dtype=torch.int64, device=dev)
+        self.d_tables = torch.empty((n, mb), dtype=torch.int32, device=dev)
+        self.d_lens = torch.empty(n, dtype=torch.int32, device=dev)
+        self.d_pairs = torch.empty((max(n, 1), 2), dtype=torch.int32, device=dev)
+        self.workspace = pkv.alloc_workspace(cache.desc, n, mb, device=dev)
+        # two pinned staging sets
+        self._stage = []
+        for _ in range(2):
+            self._stage.append(dict(
+                slots=torch.empty(n, dtype=torch.int64).pin_memory(),
+                tables=torch.empty((n, mb), dtype=torch.int32).pin_memory(),
+                lens=torch.empty(n, dtype=torch.int32).pin_memory(),
+                pairs=torch.empty((max(n, 1), 2), dtype=torch.int32).pin_memory(),
+                done=torch.cuda.Event(),
+                used=False,
+            ))
+        self._turn = 0
+        self.last_lens = np.zeros(n, dtype=np.int32)
+        self.last_n_pairs = 0
+        self.total_cow = 0
+
+    def set_sequences(self, seq_ids) -> None:
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        if len(ids) != self.n:
+            raise ValueError("batch size is fixed")
+        self.seq_ids = ids
+
+    def plan(self) -> dict:
+        """Host part of a step: reserve slots, collect CoW pairs, pack tables (pinned)."""
+        st = self._stage[self._turn]
+        self._turn ^= 1
+        if st["used"]:
+            st["done"].synchronize()  # the GPU has consumed this staging set
+        rc, slots, pairs, n_done = self.cache.mgr.append_batch(self.seq_ids)
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, f"append_batch stopped at sequence {int(self.seq_ids[n_done])}")
+        st["slots"].numpy()[:] = slots
+        npairs = len(pairs)
+        if npairs:
+            st["pairs"].numpy()[:npairs] = pairs
+        rc, _, _ = self.cache.mgr.pack_tables(self.seq_ids, self.max_blocks, st["tables"].numpy(), st["lens"].numpy())
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, "pack_tables (is max_blocks wide enough?)")
+        st["npairs"] = npairs
+        self.last_lens = st["lens"].numpy().copy()
+        self.last_n_pairs = npairs
+        self.total_cow += npairs
+        return st
+
+    def upload(self, st: dict) -> None:
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.d_slots.copy_(st["slots"], non_blocking=True)
+            self.d_tables.copy_(st["tables"], non_blocking=True)
+            self.d_lens.copy_(st["lens"], non_blocking=True)
+            if st["npairs"]:
+                self.d_pairs[: st["npairs"]].copy_(st["pairs"][: st["npairs"]], non_blocking=True)
+            st["done"].record(self.stream)
+        st["used"] = True
+
+    def run_device(self, st: dict, q, k_new, v_new, out, scale: float, on_decode=None) -> None:
+        """q/out [L, n, n_q, d]; k_new/v_new [L, n, n_kv, d] device tensors."""
+        c = self.cache
+        d = c.desc
+        if st["npairs"]:
+            pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self.d_pairs[: st["npairs"]], stream=self.stream)
+        for layer in range(d.n_layers):
+            pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], self.d_slots, c.k_pool, c.v_pool,
+                              stream=self.stream)
+            if on_decode is not None:
+                on_decode(layer, "start")
+            pkv.pkv_paged_decode_attention(d, layer, q[layer], c.k_pool, c.v_pool, self.d_tables, self.d_lens,
+                                           scale, out[layer], self.workspace, stream=self.stream)
+            if on_decode is not None:
+                on_decode(layer, "end")
+
+    def step(self, q, k_new, v_new, out, scale: float, on_decode=None) -> dict:
+        st = self.plan()
+        self.upload(st)
+        self.run_device(st, q, k_new, v_new, out, scale, on_decode)
+        return st
+
+    def kv_bytes_last_step(self) -> int:
+        """Algorithmic KV bytes the last step's attention read: sum(ctx) * 2 * n_kv * d * e * L."""
+        return int(self.last_lens.astype(np.int64).sum()) * self.cache.kv_bytes_per_token_layer() * \
+            self.cache.desc.n_layers

@@ -1,0 +1,64 @@
+"""Full-size parity, in the launch configuration bench.py times, on sampled outputs.
+
+For the gpt, ragged and longdoc workloads this builds exactly what bench.py builds (same
+pools, same batch, same table width and therefore the same grid and split-K partitions),
+runs warm-up steps plus one step, and checks sampled (layer, sequence) outputs against the
+oracle. The oracle's inputs are independent of the CUDA path: host copies of the sampled
+layers' pools taken before any step (they come from the seeded device generator), the Python
+block-manager oracle's own replay of the run, and its own byte appends of the generated rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from helpers import TOL, as_f64, to_host
+from oracle import BlockManagerOracle
+from paged_kv_cache_258_gb300 import pkv
+from paged_kv_cache_258_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+WARMUP, STEPS = 10, 100          # bench.py's defaults: they fix the table width and grid
+
+
+@pytest.mark.parametrize("config,layers,seqs", [
+    ("gpt", (0, 31), (0, 17, 40, 63)),
+    ("ragged", (0,), tuple(range(32))),
+    ("longdoc", (0, 15), (0, 9)),
+])
+def test_fullsize_sampled(config, layers, seqs):
+    device = torch.device("cuda", 0)
+    wl, _, cache, batch, (q, kn, vn, out), state = bench.setup_gpu_case(config, WARMUP, STEPS, device)
+    dtype = wl.dtype
+    host_k = {l: to_host(cache.k_pool[l], dtype) for l in layers}
+    host_v = {l: to_host(cache.v_pool[l], dtype) for l in layers}
+    # oracle replay of the admissions
+    mo = BlockManagerOracle(wl.num_blocks, free_order=W.free_order(wl.num_blocks, wl.seed))
+    for s, n in enumerate(wl.context_lens):
+        assert mo.add_seq(s, int(n) - 1)[0] == "ok"
+    n_steps = 4
+    for _ in range(n_steps):
+        st = batch.step(q, kn, vn, out, wl.scale)
+        slots = [mo.append_slot(s)[1] for s in range(wl.n_seqs)]
+        assert st["slots"].numpy().tolist() == slots
+        for l in layers:
+            oracle.kv_append(to_host(kn[l], dtype), to_host(vn[l], dtype), np.array(slots), host_k[l], host_v[l])
+    assert pkv.pkv_get_device_status() == 0
+    tables = np.full((wl.n_seqs, batch.max_blocks), -1, dtype=np.int32)
+    lens = np.zeros(wl.n_seqs, dtype=np.int32)
+    for s in range(wl.n_seqs):
+        t, lens[s] = mo.block_table(s)
+        tables[s, : len(t)] = t
+    assert np.array_equal(tables, st["tables"].numpy()) and np.array_equal(lens, st["lens"].numpy())
+    got = as_f64(out)
+    sel = np.array(seqs)
+    for l in layers:
+        ql = to_host(q[l], dtype)[sel]
+        want = oracle.paged_decode(dtype, ql, host_k[l], host_v[l], tables[sel], lens[sel], wl.scale,
+                                   n_threads=oracle.max_threads())
+        err = np.max(np.abs(got[l][sel] - want))
+        assert err <= TOL[dtype], f"{config} layer {l}: max abs error {err:.3e}"
+    # every output row of the step is finite
+    assert torch.isfinite(out.float()).all()
