@@ -149,8 +149,17 @@ def measured_peaks() -> dict:
 # ---------------------------------------------------------------------------------------------
 # workloads
 
-def build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
-    """(workload, initial prompt per sequence, churn log or None)."""
+def build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0, layers: int | None = None):
+    """(workload, description, churn log or None). ``layers`` overrides the layer count only
+    (every layer's launch is identical, so a 2-layer case profiles the same kernel launch)."""
+    wl, desc, churn = _build_workload(name, warmup, steps, seed_offset)
+    if layers is not None and layers != wl.n_layers:
+        wl.n_layers = int(layers)
+        desc += f" [reduced to {layers} layers]"
+    return wl, desc, churn
+
+
+def _build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
     extra = warmup + 2 * steps + 2 * W.BLOCK
     if name == "gpt":
         wl = W.gpt(seed=W.BASE_SEED + 1 + seed_offset, extra_tokens_per_seq=extra)
@@ -176,12 +185,12 @@ def build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
     return wl, desc, None
 
 
-def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int = 0):
+def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int = 0, layers: int | None = None):
     import torch
     from paged_kv_cache_258_gb300 import pkv
     from paged_kv_cache_258_gb300.engine import DecodeBatch, PagedKVCache
 
-    wl, wdesc, churn = build_workload(name, warmup, steps, seed_offset)
+    wl, wdesc, churn = build_workload(name, warmup, steps, seed_offset, layers)
     desc = pkv.make_desc(wl.dtype, wl.n_layers, wl.num_blocks, wl.n_q_heads, wl.n_kv_heads, wl.head_dim)
     cache = PagedKVCache(desc, free_order=W.free_order(wl.num_blocks, wl.seed), device=device, init="randn",
                          seed=wl.seed)
@@ -240,7 +249,7 @@ def run_gpu(args) -> dict | None:
     device = torch.device("cuda", local)
     pkv.lib()
     wl, wdesc, cache, batch, (q, k_new, v_new, out), state = setup_gpu_case(
-        args.config, args.warmup, args.steps, device, seed_offset=rank)
+        args.config, args.warmup, args.steps, device, seed_offset=rank, layers=args.layers)
     stream = batch.stream
     scale = wl.scale
 
@@ -276,12 +285,9 @@ def run_gpu(args) -> dict | None:
     launches0 = pkv.pkv_launch_count()
     kv_bytes = 0
     cow_pairs = 0
-    host_plan_s = 0.0
     t0.record(stream)
     for _ in range(args.steps):
-        h0 = time.perf_counter()
         st = batch.plan()
-        host_plan_s += time.perf_counter() - h0
         batch.upload(st)
         batch.run_device(st, q, k_new, v_new, out, scale, on_decode)
         b = batch.kv_bytes_last_step()
@@ -357,7 +363,7 @@ def run_gpu(args) -> dict | None:
         },
         "e2e": e2e,
         "gpu_launches": int(launches),
-        "host_plan_us_per_step": round(host_plan_s / args.steps * 1e6, 1),
+        "host_manager_us_per_step": round(batch.manager_s / max(batch.steps_planned, 1) * 1e6, 1),
         "cow_pairs_timed": int(cow_pairs),
         "clocks": clocks,
     }
@@ -521,6 +527,7 @@ def main(argv=None):
     ap.add_argument("--config", default="gpt", choices=["gpt", "ragged", "longdoc", "prefix"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -17,6 +17,8 @@ All device work is in libpkv's kernels; this module only moves arguments.
 """
 from __future__ import annotations
 
+import time
+
 import numpy as np
 
 from . import pkv
@@ -93,6 +95,8 @@ class DecodeBatch:
         self.last_lens = np.zeros(n, dtype=np.int32)
         self.last_n_pairs = 0
         self.total_cow = 0
+        self.manager_s = 0.0       # host time in the block manager (append + pack), waits excluded
+        self.steps_planned = 0
 
     def set_sequences(self, seq_ids) -> None:
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
@@ -106,6 +110,7 @@ class DecodeBatch:
         self._turn ^= 1
         if st["used"]:
             st["done"].synchronize()  # the GPU has consumed this staging set
+        t0 = time.perf_counter()
         rc, slots, pairs, n_done = self.cache.mgr.append_batch(self.seq_ids)
         if rc != pkv.PKV_OK:
             raise pkv.PkvError(rc, f"append_batch stopped at sequence {int(self.seq_ids[n_done])}")
@@ -117,6 +122,8 @@ class DecodeBatch:
         if rc != pkv.PKV_OK:
             raise pkv.PkvError(rc, "pack_tables (is max_blocks wide enough?)")
         st["npairs"] = npairs
+        self.manager_s += time.perf_counter() - t0
+        self.steps_planned += 1
         self.last_lens = st["lens"].numpy().copy()
         self.last_n_pairs = npairs
         self.total_cow += npairs
