@@ -428,7 +428,7 @@ def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "paged_kv_cache_258_gb300" / "csrc"
-    for name in ("decode.cuh", "common.cuh", "internal.h"):
+    for name in ("decode.cuh", "common.cuh"):
         h.update((csrc / name).read_bytes())
     return h.hexdigest()
 
