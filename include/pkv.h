@@ -154,6 +154,35 @@ int pkv_paged_decode_attention(const pkv_cache_desc* desc, int32_t layer, const 
                                float scale, void* out, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Size of the fixed scratch array used by pkv_paged_decode_attention_static (16 MiB). */
+#define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * pkv_paged_decode_attention without a workspace argument, for callers that cannot allocate
+ * device memory when they run attention (code inside a stream capture, a serving loop that
+ * forbids allocation after start-up, an embedding host with a fixed memory budget). The pages
+ * have no counterpart: this is an interface convenience, not part of the method.
+ * Same arguments, layout, result and errors as pkv_paged_decode_attention minus workspace and
+ * workspace_bytes. The split-K partial results go to a scratch array of
+ * PKV_STATIC_SCRATCH_BYTES compiled into the library; every GPU that loads the library holds
+ * it until the process exits. The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   - Returns PKV_ERR_UNSUPPORTED, launching nothing, when the call would need more than
+ *     PKV_STATIC_SCRATCH_BYTES (when pkv_decode_workspace_bytes(desc, n_seqs,
+ *     max_blocks_per_seq) exceeds it); use pkv_paged_decode_attention with your own workspace.
+ *   - The first call on each device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls share the one array and it keeps the last call's contents (which no call
+ *     reads: every partial result is written before it is combined, so nothing needs
+ *     clearing). Calls that overlap on the GPU -- on different streams, or from several host
+ *     threads -- race on it: serialise them.
+ */
+int pkv_paged_decode_attention_static(const pkv_cache_desc* desc, int32_t layer, const void* q,
+                                      const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
+                                      float scale, void* out, void* stream);
+
 /*
  * Copy-on-write block copies ("01 - Conceito", paragraph 6): for each pair (src, dst) in
  * pairs (device int32 [n_pairs][2]) copy physical block src onto dst in K and V, all layers.

@@ -62,6 +62,10 @@ int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
     return bpp;
 }
 
+cudaError_t device_status_word(unsigned int** out) { return status_word(out); }
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
 cudaError_t launch_decode(int dtype, int head_dim, int group, const DecodeArgs& a, cudaStream_t stream,
                           int* n_launches) {
     switch (dtype) {

@@ -63,4 +63,9 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const DecodeArgs& a, cud
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 
+// Shared with decode_static.cu (abi.cu owns both): the current device's status word, and the
+// process-wide count of kernels launched by this library.
+cudaError_t device_status_word(unsigned int** out);
+void count_launches(uint64_t n);
+
 }  // namespace pkv

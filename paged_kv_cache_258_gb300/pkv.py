@@ -70,6 +70,8 @@ def lib():
         "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
         "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
                                                       vp, vp, c_sz, vp]),
+        "pkv_paged_decode_attention_static": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32,
+                                                             ctypes.c_float, vp, vp]),
         "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
@@ -196,6 +198,29 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
         _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
         _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
     _check(rc, "pkv_paged_decode_attention")
+
+
+def pkv_paged_decode_attention_static(desc: CacheDesc, layer: int, q, k_pool, v_pool, block_tables, context_lens,
+                                      scale: float, out, stream=None) -> None:
+    """pkv_paged_decode_attention with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory when attention runs; see include/pkv.h
+    for the scratch limit and the rule that overlapping calls must be serialised.
+    """
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_seqs = int(q.shape[0])
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [n_seqs, max_blocks]")
+    max_blocks = int(block_tables.shape[1])
+    qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
+    rc = lib().pkv_paged_decode_attention_static(
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
+        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape), _stream_handle(stream))
+    _check(rc, "pkv_paged_decode_attention_static")
 
 
 def pkv_copy_blocks(desc: CacheDesc, k_pool, v_pool, pairs, stream=None) -> None:
