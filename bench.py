@@ -350,7 +350,8 @@ def run_gpu(args) -> dict | None:
         "hbm_frac_of_measured": round(value / hbm_peak, 4),
         "hbm_frac_of_nominal_7900": round(value / NOMINAL_HBM_GBS, 4),
         "roofline": {
-            "kernel": "paged_decode_kernel (+ splitk_combine_kernel when a sequence has several partitions)",
+            "kernel": ("paged_decode_mma_kernel" if wl.dtype != "f32" else "paged_decode_kernel")
+                      + " (+ splitk_combine_kernel when a sequence has several partitions)",
             "bound": "hbm",
             "achieved": round(achieved_gbs, 2),
             "peak": hbm_peak,
@@ -428,7 +429,7 @@ def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "paged_kv_cache_258_gb300" / "csrc"
-    for name in ("decode.cuh", "common.cuh"):
+    for name in ("decode.cuh", "decode_mma.cuh", "common.cuh"):
         h.update((csrc / name).read_bytes())
     return h.hexdigest()
 

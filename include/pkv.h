@@ -107,7 +107,8 @@ uint64_t pkv_pool_bytes(const pkv_cache_desc* desc);
 
 /*
  * Scratch bytes pkv_paged_decode_attention needs for n_seqs sequences whose tables have
- * max_blocks_per_seq columns (split-K partial results; 0 when no split is needed).
+ * max_blocks_per_seq columns: split-K partial results plus one 8-byte arrival counter per
+ * (sequence, KV head); 0 when no split is needed.
  */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq);
 
@@ -143,7 +144,10 @@ int pkv_kv_append(const pkv_cache_desc* desc, int32_t layer, const void* k, cons
  *   context_lens  device int32 [n_seqs], 0 <= len <= max_blocks_per_seq*16 (a larger one
  *                 is clamped and sets PKV_DEV_BAD_CONTEXT_LEN)
  *   workspace     device, >= pkv_decode_workspace_bytes(...) bytes, 16-byte aligned
- *                 (may be NULL when that is 0); contents need no initialisation
+ *                 (may be NULL when that is 0); contents need no initialisation (the split-K
+ *                 arrival counters kept there carry a per-call tag, so leftovers of earlier
+ *                 calls of any shape read as zero). Calls that overlap on the GPU must not
+ *                 share one workspace.
  * Rows outside the valid positions (tails of last blocks, unreferenced blocks) are never
  * used: NaN there cannot reach the output. A table entry outside [0, num_blocks) is
  * skipped (its rows count as masked) and sets PKV_DEV_BAD_BLOCK_ID.
@@ -153,6 +157,25 @@ int pkv_paged_decode_attention(const pkv_cache_desc* desc, int32_t layer, const 
                                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
                                float scale, void* out, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/*
+ * One decode step of one layer in a single kernel: pkv_kv_append of one new token per sequence
+ * followed by pkv_paged_decode_attention. The token of sequence s sits at logical position
+ * context_lens[s] - 1 ("La idea de PagedAttention", step 3: written into the last block, which
+ * the block manager has already reserved -- pkv_mgr_append_slot's slot), so its slot follows
+ * from the table: block_tables[s][(len-1)/16] * 16 + (len-1) % 16. The rows
+ * k_new[s][g], v_new[s][g] (device, [n_seqs][n_kv_heads][head_dim] of desc->dtype, 16-byte
+ * aligned) are written there in layer `layer` of the pools, then the sequence attends to its
+ * first context_lens[s] positions, the new one included. Results (pools and out) are
+ * bit-identical to the two separate calls. Other arguments, layout and errors as
+ * pkv_paged_decode_attention; k_pool / v_pool are written. Sequences with context_lens[s] == 0
+ * append nothing. Copy-on-write block copies for this step must already have run.
+ */
+int pkv_paged_decode_append_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
+                                      const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t n_seqs, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the fixed scratch array used by pkv_paged_decode_attention_static (16 MiB). */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
@@ -173,10 +196,11 @@ int pkv_paged_decode_attention(const pkv_cache_desc* desc, int32_t layer, const 
  *   - The first call on each device looks up the scratch array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call before any stream
  *     capture begins.
- *   - All calls share the one array and it keeps the last call's contents (which no call
- *     reads: every partial result is written before it is combined, so nothing needs
- *     clearing). Calls that overlap on the GPU -- on different streams, or from several host
- *     threads -- race on it: serialise them.
+ *   - All calls share the one array and it keeps the last call's contents. No call reads an
+ *     earlier call's partial results (each is written before it is merged), and the split-K
+ *     arrival counters kept there carry a per-call tag, so leftovers of earlier calls of any
+ *     shape read as zero: nothing needs clearing. Calls that overlap on the GPU -- on
+ *     different streams, or from several host threads -- race on it: serialise them.
  */
 int pkv_paged_decode_attention_static(const pkv_cache_desc* desc, int32_t layer, const void* q,
                                       const void* k_pool, const void* v_pool, const int32_t* block_tables,

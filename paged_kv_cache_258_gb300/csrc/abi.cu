@@ -38,26 +38,31 @@ size_t layer_elems(const pkv_cache_desc* d) {
     return (size_t)d->num_blocks * d->n_kv_heads * d->block_size * d->head_dim;
 }
 
-size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int* bpp_out, int* n_parts_out) {
+size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int* bpp_out, int* n_parts_out,
+                        size_t* off_ml = nullptr, size_t* off_cnt = nullptr) {
     const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks);
     const int n_parts = pkv::decode_partitions(max_blocks, bpp);
     if (bpp_out) *bpp_out = bpp;
     if (n_parts_out) *n_parts_out = n_parts;
-    if (n_parts <= 1) return 0;
-    return (size_t)n_seqs * d->n_q_heads * n_parts * (d->head_dim + 2) * sizeof(float);
+    size_t ml = 0, cnt = 0;
+    const size_t bytes =
+        pkv::decode_workspace_layout(n_seqs, d->n_q_heads, d->n_kv_heads, d->head_dim, n_parts, &ml, &cnt);
+    if (off_ml) *off_ml = ml;
+    if (off_cnt) *off_cnt = cnt;
+    return bytes;
 }
 
 }  // namespace
 
 namespace pkv {
 
-// Blocks per partition: 32 (512 tokens) unless the grid would then hold fewer than ~4 CTAs per
+// Blocks per partition: 64 (1,024 tokens) unless the grid would then hold fewer than ~4 CTAs per
 // SM of a GB300 (152 SMs), in which case partitions shrink (down to 4 blocks) to spread one
 // long sequence over more SMs. Depends only on the arguments, so the workspace query and the
 // launch agree on every device.
 int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
     const long long target = 4LL * 152;
-    int bpp = 32;
+    int bpp = 64;
     while (bpp > 4 && (long long)n_seqs * n_kv * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
     return bpp;
 }
@@ -65,6 +70,15 @@ int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
 cudaError_t device_status_word(unsigned int** out) { return status_word(out); }
 
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+unsigned long long next_call_tag() {
+    static std::atomic<unsigned long long> tag{0};
+    unsigned long long t;
+    do {
+        t = (tag.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
+    } while (t == 0);
+    return t;
+}
 
 cudaError_t launch_decode(int dtype, int head_dim, int group, const DecodeArgs& a, cudaStream_t stream,
                           int* n_launches) {
@@ -146,10 +160,11 @@ int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const v
     return PKV_OK;
 }
 
-int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
-                               const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                               const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+// Shared body of the two decode entry points; k_new / v_new are null unless the append is fused.
+static int decode_call(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new, const void* v_new,
+                       const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
     int rc = pkv_validate_desc(d);
     if (rc != PKV_OK) return rc;
     if (layer < 0 || layer >= d->n_layers || n_seqs < 0) return PKV_ERR_INVALID_ARG;
@@ -158,8 +173,10 @@ int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const voi
     if (n_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+    if ((k_new || v_new) && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
     int bpp = 0, n_parts = 0;
-    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, &bpp, &n_parts);
+    size_t off_ml = 0, off_cnt = 0;
+    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, &bpp, &n_parts, &off_ml, &off_cnt);
     if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
 
     pkv::DecodeArgs a;
@@ -170,8 +187,12 @@ int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const voi
     a.tables = block_tables;
     a.lens = context_lens;
     a.out = out;
-    a.part_o = static_cast<float*>(workspace);
-    a.part_ml = need ? a.part_o + (size_t)n_seqs * d->n_q_heads * n_parts * d->head_dim : nullptr;
+    a.part_o = need ? static_cast<float*>(workspace) : nullptr;
+    a.part_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + off_ml) : nullptr;
+    a.counters = need ? reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + off_cnt) : nullptr;
+    a.call_tag = pkv::next_call_tag();
+    a.k_new = k_new;
+    a.v_new = v_new;
     a.n_seqs = n_seqs;
     a.n_q = d->n_q_heads;
     a.n_kv = d->n_kv_heads;
@@ -186,6 +207,23 @@ int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const voi
                                          static_cast<cudaStream_t>(stream), &launches);
     g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
     return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return decode_call(d, layer, q, nullptr, nullptr, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                       n_seqs, scale, out, workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_decode_append_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new,
+                                      const void* v_new, void* k_pool, void* v_pool, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
+                                      float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (n_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+    return decode_call(d, layer, q, k_new, v_new, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                       n_seqs, scale, out, workspace, workspace_bytes, stream);
 }
 
 int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,

@@ -147,6 +147,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy global writes before later async-proxy (TMA) reads
+// of the same global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- warp reductions -------------------------------------------------------------------------
 // Sum N values per lane across aligned groups of 2*O lanes, halving the values kept per lane at
 // each step (a transpose-reduce): after the call, lane L of its group holds the complete sums of

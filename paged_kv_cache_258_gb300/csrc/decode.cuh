@@ -26,7 +26,9 @@
 //    in unused rows cannot leak into the result.
 //  * At the end the warps' states are merged in shared memory. A sequence with a single
 //    partition writes its final row directly; otherwise the CTA writes an unnormalised partial
-//    (o, max, sum) and a second small kernel merges the partitions (log-sum-exp combine).
+//    (o, max, sum) to the workspace, and the CTA that finishes last among the sequence's
+//    partitions (an arrival counter per sequence and KV head) merges them (log-sum-exp combine)
+//    inside the same kernel -- no second launch.
 #pragma once
 
 #include <math.h>
@@ -58,6 +60,14 @@ struct DecodeTuning {
     static constexpr int ST = NW * 2 * STAGE_BYTES > 200 * 1024 ? 1 : (ST_RAW < 2 ? 2 : (ST_RAW > 4 ? 4 : ST_RAW));
 };
 
+constexpr int kMergeChunk = 32;  // partitions whose weights are staged in shared memory at a time
+
+// Shared-memory floats the split-K merge needs (flag, row maxima, row sums, one chunk of weights).
+template <int G>
+struct MergeScratch {
+    static constexpr size_t BYTES = (4 + 2 * G + G * kMergeChunk) * sizeof(float);
+};
+
 template <typename T, int D, int G, int NW, int ST>
 struct DecodeSmem {
     using Geo = RowGeom<T, D>;
@@ -68,8 +78,130 @@ struct DecodeSmem {
     static constexpr size_t PBUF = ZBUF + (size_t)NW * G * kBlock * 4;    // float [NW][G*16]
     static constexpr size_t ML = PBUF + (size_t)NW * G * kBlock * 4;      // float [NW][G][2]
     static constexpr size_t TOTAL = ML + (size_t)NW * G * 2 * 4;
-    static_assert((size_t)NW * G * D * 4 <= STAGES, "combine buffer must fit in the stage area");
+    static constexpr size_t MERGE = ((size_t)NW * G * D * 4 + 15) / 16 * 16;  // merge scratch, after the combine buffer
+    static_assert(MERGE + MergeScratch<G>::BYTES <= STAGES, "combine buffer and merge scratch must fit in the stage area");
 };
+
+// Split-K epilogue of the CTA (s, g, p) of a sequence with np > 1 partitions, after the CTA has
+// stored its unnormalised partial (o, max, sum) for its G query rows. The CTA that arrives last at
+// the (s, g) counter merges the np partials of every row -- o = sum_p o_p 2^(m_p - M) / sum_p l_p
+// 2^(m_p - M), M = max_p m_p -- and writes the output rows.
+// The counter holds (call tag << 24) | arrivals. A value carrying another tag (a finished call,
+// a zeroed or never-initialised buffer, another geometry's partials) counts as zero arrivals, so
+// the workspace needs no clearing; the merging CTA resets the counter to 0, so a replay of an
+// identical launch also starts from zero. One thread per CTA publishes the CTA's writes (barrier,
+// then fence, then the atomic) and the merging CTA reads the partials from L2 after a fence. The
+// merge order is fixed, so the result does not depend on which CTA happens to finish last.
+template <typename T, int D, int G, int NT>
+__device__ __forceinline__ void splitk_merge_if_last(const DecodeArgs& a, int s, int g, int np, float* scratch) {
+    static_assert(NT % 32 == 0, "whole warps");
+    constexpr int NWARP = NT / 32;
+    constexpr int PER = (G * D + NT - 1) / NT;
+    int* flag = reinterpret_cast<int*>(scratch);
+    float* sM = scratch + 4;  // [G]
+    float* sL = sM + G;       // [G]
+    float* sW = sL + G;       // [G][kMergeChunk]
+    unsigned long long* cnt = a.counters + (size_t)s * a.n_kv + g;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
+        unsigned long long next;
+        while (true) {
+            next = ((cur >> 24) == a.call_tag) ? cur + 1 : ((a.call_tag << 24) | 1ull);
+            const unsigned long long prev = atomicCAS(cnt, cur, next);
+            if (prev == cur) break;
+            cur = prev;
+        }
+        *flag = (next & 0xffffffull) == (unsigned long long)np;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!*flag) return;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const size_t row0 = (size_t)s * a.n_q + (size_t)g * G;
+    for (int r = warp; r < G; r += NWARP) {
+        const float* ml = a.part_ml + (row0 + r) * a.n_parts * 2;
+        float m = -INFINITY;
+        for (int q = lane; q < np; q += 32) m = fmaxf(m, __ldcg(ml + 2 * q));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            sM[r] = m;
+            sL[r] = 0.f;
+        }
+    }
+    float O[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) O[k] = 0.f;
+    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
+        __syncthreads();  // maxima visible; the previous chunk's weights consumed
+        for (int r = warp; r < G; r += NWARP) {
+            const float* ml = a.part_ml + (row0 + r) * a.n_parts * 2;
+            const int q = c0 + lane;
+            float w = 0.f, lw = 0.f;
+            if (q < np) {
+                const float m = __ldcg(ml + 2 * q);
+                if (m != -INFINITY) {
+                    w = exp2f(m - sM[r]);
+                    lw = __ldcg(ml + 2 * q + 1) * w;
+                }
+            }
+            sW[r * kMergeChunk + lane] = w;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+            if (lane == 0) sL[r] += lw;
+        }
+        __syncthreads();
+        const int nq = min(kMergeChunk, np - c0);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = threadIdx.x + k * NT;
+            if (idx < G * D) {
+                const int r = idx / D;
+                const int d = idx % D;
+                const float* po = a.part_o + ((row0 + r) * a.n_parts + c0) * D + d;
+                for (int q = 0; q < nq; ++q) O[k] = fmaf(sW[r * kMergeChunk + q], __ldcg(po + (size_t)q * D), O[k]);
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int idx = threadIdx.x + k * NT;
+        if (idx < G * D) {
+            const int r = idx / D;
+            const int d = idx % D;
+            const float L = sL[r];
+            reinterpret_cast<T*>(a.out)[(row0 + r) * D + d] = from_float<T>(L > 0.f ? O[k] / L : 0.f);
+        }
+    }
+    if (threadIdx.x == 0) *cnt = 0ull;
+}
+
+// Fused KV append (decode step): the CTA whose partition holds the sequence's last block writes the
+// new token's K and V rows of its KV head g at position ctx-1 -- slot table[nb-1]*16 + (ctx-1)%16,
+// the slot the block manager reserved -- before any of its TMA loads, then fences the generic
+// writes against the asynchronous proxy. No other CTA reads that block. An out-of-range block id
+// writes nothing (the attention path skips and flags that block).
+template <typename T, int D, int NT>
+__device__ __forceinline__ void fused_append(const DecodeArgs& a, int s, int g, int p, int ctx, int nb) {
+    if (a.k_new == nullptr || p != (nb - 1) / a.bpp) return;
+    const int phys = a.tables[(size_t)s * a.max_blocks + nb - 1];
+    if ((unsigned)phys >= (unsigned)a.num_blocks) return;
+    constexpr int NCH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
+    const size_t src_row = ((size_t)s * a.n_kv + g) * D;
+    const size_t dst_row = (((size_t)phys * a.n_kv + g) * kBlock + (ctx - 1) % kBlock) * D;
+    for (int i = threadIdx.x; i < 2 * NCH; i += NT) {
+        const bool is_v = i >= NCH;
+        const int c = is_v ? i - NCH : i;
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(is_v ? a.v_new : a.k_new) + src_row) + c;
+        uint4* dst = reinterpret_cast<uint4*>(const_cast<T*>(reinterpret_cast<const T*>(is_v ? a.v_layer : a.k_layer)) + dst_row) + c;
+        *dst = __ldg(src);
+    }
+    fence_proxy_async_global();
+}
 
 template <typename T, int D, int G, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs a) {
@@ -115,6 +247,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
     }
     const int nblk = min(a.bpp, nb - b0);
     const bool single = nb <= a.bpp;
+    fused_append<T, D, NW * 32>(a, s, g, p, ctx, nb);
 
     if (threadIdx.x < NW * ST) mbar_init(&bars[threadIdx.x], 1);
     fence_mbar_init();
@@ -376,43 +509,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
             }
         }
     }
-}
-
-// Log-sum-exp merge of a sequence's partitions: grid (n_q, n_seqs), D/4 threads, 4 dims each.
-template <typename T, int D>
-__global__ void __launch_bounds__(D / 4) splitk_combine_kernel(const DecodeArgs a) {
-    const int h = blockIdx.x;
-    const int s = blockIdx.y;
-    int ctx = a.lens[s];
-    const int cap = a.max_blocks * kBlock;
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int nb = (ctx + kBlock - 1) / kBlock;
-    const int np = (nb + a.bpp - 1) / a.bpp;
-    if (np <= 1) return;  // written directly by the decode kernel
-    const size_t row = (size_t)s * a.n_q + h;
-    const float* ml = a.part_ml + row * a.n_parts * 2;
-    float M = -INFINITY;
-    for (int q = 0; q < np; ++q) M = fmaxf(M, ml[2 * q]);
-    const int d = threadIdx.x * 4;
-    float L = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < np; ++q) {
-        const float mq = ml[2 * q];
-        if (mq == -INFINITY) continue;
-        const float w = exp2f(mq - M);
-        L = fmaf(ml[2 * q + 1], w, L);
-        const float4 o = *reinterpret_cast<const float4*>(a.part_o + (row * a.n_parts + q) * D + d);
-        O.x = fmaf(o.x, w, O.x);
-        O.y = fmaf(o.y, w, O.y);
-        O.z = fmaf(o.z, w, O.z);
-        O.w = fmaf(o.w, w, O.w);
-    }
-    T* out = reinterpret_cast<T*>(a.out) + row * D + d;
-    const bool ok = L > 0.f;
-    out[0] = from_float<T>(ok ? O.x / L : 0.f);
-    out[1] = from_float<T>(ok ? O.y / L : 0.f);
-    out[2] = from_float<T>(ok ? O.z / L : 0.f);
-    out[3] = from_float<T>(ok ? O.w / L : 0.f);
+    if (!single)
+        splitk_merge_if_last<T, D, G, NW * 32>(a, s, g, (nb + a.bpp - 1) / a.bpp,
+                                               reinterpret_cast<float*>(smem + S::MERGE));
 }
 
 template <typename T, int D, int G>
@@ -432,15 +531,8 @@ cudaError_t launch_decode_tpl(const DecodeArgs& a, cudaStream_t stream, int* n_l
     }
     dim3 grid(a.n_parts, a.n_kv, a.n_seqs);
     kern<<<grid, NW * 32, smem, stream>>>(a);
-    int launches = 1;
-    err = cudaGetLastError();
-    if (err == cudaSuccess && a.n_parts > 1) {
-        splitk_combine_kernel<T, D><<<dim3(a.n_q, a.n_seqs), D / 4, 0, stream>>>(a);
-        launches++;
-        err = cudaGetLastError();
-    }
-    if (n_launches) *n_launches = launches;
-    return err;
+    if (n_launches) *n_launches = 1;
+    return cudaGetLastError();
 }
 
 template <typename T>

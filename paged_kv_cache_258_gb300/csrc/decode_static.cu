@@ -65,8 +65,9 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     // Same partition geometry, hence the same scratch need, as pkv_paged_decode_attention.
     const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks_per_seq);
     const int n_parts = pkv::decode_partitions(max_blocks_per_seq, bpp);
+    size_t off_ml = 0, off_cnt = 0;
     const size_t need =
-        n_parts > 1 ? (size_t)n_seqs * d->n_q_heads * n_parts * (d->head_dim + 2) * sizeof(float) : 0;
+        pkv::decode_workspace_layout(n_seqs, d->n_q_heads, d->n_kv_heads, d->head_dim, n_parts, &off_ml, &off_cnt);
     if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_UNSUPPORTED;  // too big for the fixed scratch
 
     float* scratch = nullptr;
@@ -81,10 +82,13 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     a.tables = block_tables;
     a.lens = context_lens;
     a.out = out;
-    // Every partial row the combine step reads is written earlier in the same call, so the
-    // scratch needs no clearing and stale contents from an earlier call are never read.
-    a.part_o = scratch;
-    a.part_ml = need ? scratch + (size_t)n_seqs * d->n_q_heads * n_parts * d->head_dim : nullptr;
+    // Every partial the merge reads is written earlier in the same call, so stale partials from an
+    // earlier call are never read; the arrival counters carry this call's tag, so whatever an
+    // earlier call left in the array (counters or partials of another geometry) reads as zero.
+    a.part_o = need ? scratch : nullptr;
+    a.part_ml = need ? reinterpret_cast<float*>(reinterpret_cast<char*>(scratch) + off_ml) : nullptr;
+    a.counters = need ? reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(scratch) + off_cnt) : nullptr;
+    a.call_tag = pkv::next_call_tag();
     a.n_seqs = n_seqs;
     a.n_q = d->n_q_heads;
     a.n_kv = d->n_kv_heads;

@@ -1,6 +1,7 @@
 // internal.h -- declarations shared by the library's translation units (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,6 +23,10 @@ struct DecodeArgs {
     void* out;              // [n_seqs][n_q][D]
     float* part_o;          // [n_seqs][n_q][n_parts][D]   (split-K only)
     float* part_ml;         // [n_seqs][n_q][n_parts][2]   (running max, sum)
+    unsigned long long* counters = nullptr;  // [n_seqs][n_kv] partition arrivals: (call tag << 24) | count
+    unsigned long long call_tag = 0;         // 1 .. 2^40-1, distinct for consecutive calls
+    const void* k_new = nullptr;       // fused append: [n_seqs][n_kv][D] rows of position ctx-1,
+    const void* v_new = nullptr;       // written before attention; nullptr = no append
     unsigned int* status;   // device status word
     int n_seqs, n_q, n_kv, num_blocks, max_blocks;
     int n_parts;            // partitions per sequence row of the grid
@@ -54,6 +59,21 @@ struct CopyArgs {
 int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks);
 inline int decode_partitions(int max_blocks, int bpp) { return (max_blocks + bpp - 1) / bpp; }
 
+// Split-K workspace layout (0 bytes when n_parts <= 1): fp32 partial outputs
+// [n_seqs][n_q][n_parts][D], then (max, sum) pairs [n_seqs][n_q][n_parts][2] at *off_ml, then the
+// 64-bit arrival counters [n_seqs][n_kv] at *off_cnt (16-byte aligned). Returns the total bytes.
+inline size_t decode_workspace_layout(int n_seqs, int n_q, int n_kv, int head_dim, int n_parts, size_t* off_ml,
+                                      size_t* off_cnt) {
+    *off_ml = *off_cnt = 0;
+    if (n_parts <= 1) return 0;
+    const size_t o = (size_t)n_seqs * n_q * n_parts * head_dim * sizeof(float);
+    const size_t ml = (size_t)n_seqs * n_q * n_parts * 2 * sizeof(float);
+    const size_t cnt = (size_t)n_seqs * n_kv * sizeof(unsigned long long);
+    *off_ml = o;
+    *off_cnt = (o + ml + 15) / 16 * 16;
+    return *off_cnt + (cnt + 15) / 16 * 16;
+}
+
 // Launchers (decode_*.cu, append_copy.cu). Return the first CUDA error, or cudaSuccess.
 cudaError_t launch_decode(int dtype, int head_dim, int group, const DecodeArgs& a, cudaStream_t stream,
                           int* n_launches);
@@ -63,9 +83,21 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const DecodeArgs& a, cud
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 
+// Tensor-core decode (decode_mma.cuh) serves 16-bit storage when G >= kMmaMinGroup and the pool's
+// rows fit the 32-bit TMA row coordinate; everything else runs the CUDA-core kernel (decode.cuh).
+constexpr int kMmaMinGroup = 1;
+inline bool decode_uses_mma(int dtype, int group, long long rows) {
+    return dtype != PKV_F32 && group >= kMmaMinGroup && rows < (1LL << 31);
+}
+
+// Cached TMA tensor map of one pool layer seen as rows x head_dim 16-bit elements (tmap.cu).
+cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, CUtensorMap* out);
+
 // Shared with decode_static.cu (abi.cu owns both): the current device's status word, and the
 // process-wide count of kernels launched by this library.
 cudaError_t device_status_word(unsigned int** out);
 void count_launches(uint64_t n);
+// A fresh tag for one decode call's split-K arrival counters (never 0, wraps below 2^40).
+unsigned long long next_call_tag();
 
 }  // namespace pkv

@@ -11,7 +11,8 @@ method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAtten
              double-buffered so the host can plan step i+1 while step i's copy is pending);
   3. device: copy-on-write block copies, then per layer the KV append and the paged decode
              attention -- copies before appends (else a copy would overwrite the new row),
-             appends before attention (the new token attends to itself).
+             appends before attention (the new token attends to itself). By default the append
+             and the attention of a layer are one kernel (pkv_paged_decode_append_attention).
 
 All device work is in libpkv's kernels; this module only moves arguments.
 """
@@ -65,13 +66,15 @@ class PagedKVCache:
 class DecodeBatch:
     """Decode steps for a batch of n sequences whose tables are at most max_blocks wide."""
 
-    def __init__(self, cache: PagedKVCache, seq_ids, max_blocks: int, stream=None):
+    def __init__(self, cache: PagedKVCache, seq_ids, max_blocks: int, stream=None, fused: bool = True):
         import torch
         self.cache = cache
         self.seq_ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         self.n = len(self.seq_ids)
         self.max_blocks = int(max_blocks)
         self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
+        # fused: one kernel per layer appends the new rows and attends; else kv_append + decode
+        self.fused = bool(fused)
         dev = cache.device
         n, mb = self.n, self.max_blocks
         # device metadata (fixed addresses: the launches see the same pointers every step)
@@ -147,12 +150,19 @@ class DecodeBatch:
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self.d_pairs[: st["npairs"]], stream=self.stream)
         for layer in range(d.n_layers):
-            pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], self.d_slots, c.k_pool, c.v_pool,
-                              stream=self.stream)
-            if on_decode is not None:
-                on_decode(layer, "start")
-            pkv.pkv_paged_decode_attention(d, layer, q[layer], c.k_pool, c.v_pool, self.d_tables, self.d_lens,
-                                           scale, out[layer], self.workspace, stream=self.stream)
+            if self.fused:
+                if on_decode is not None:
+                    on_decode(layer, "start")
+                pkv.pkv_paged_decode_append_attention(d, layer, q[layer], k_new[layer], v_new[layer], c.k_pool,
+                                                      c.v_pool, self.d_tables, self.d_lens, scale, out[layer],
+                                                      self.workspace, stream=self.stream)
+            else:
+                pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], self.d_slots, c.k_pool, c.v_pool,
+                                  stream=self.stream)
+                if on_decode is not None:
+                    on_decode(layer, "start")
+                pkv.pkv_paged_decode_attention(d, layer, q[layer], c.k_pool, c.v_pool, self.d_tables, self.d_lens,
+                                               scale, out[layer], self.workspace, stream=self.stream)
             if on_decode is not None:
                 on_decode(layer, "end")
 

@@ -70,6 +70,8 @@ def lib():
         "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
         "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
                                                       vp, vp, c_sz, vp]),
+        "pkv_paged_decode_append_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, vp, vp, c_i32, vp, c_i32,
+                                                             ctypes.c_float, vp, vp, c_sz, vp]),
         "pkv_paged_decode_attention_static": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32,
                                                              ctypes.c_float, vp, vp]),
         "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
@@ -200,6 +202,31 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
     _check(rc, "pkv_paged_decode_attention")
 
 
+def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_new, k_pool, v_pool, block_tables,
+                                      context_lens, scale: float, out, workspace=None, stream=None) -> None:
+    """One decode step of one layer: append each sequence's new K/V row at position len-1, then attend."""
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_seqs = int(q.shape[0])
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [n_seqs, max_blocks]")
+    max_blocks = int(block_tables.shape[1])
+    qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
+    kvshape = (n_seqs, desc.n_kv_heads, desc.head_dim)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pkv_paged_decode_append_attention(
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape), _dev(k_new, "k_new", dt, kvshape),
+        _dev(v_new, "v_new", dt, kvshape), _dev(k_pool, "k_pool", dt, pool_shape(desc)),
+        _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(rc, "pkv_paged_decode_append_attention")
+
+
 def pkv_paged_decode_attention_static(desc: CacheDesc, layer: int, q, k_pool, v_pool, block_tables, context_lens,
                                       scale: float, out, stream=None) -> None:
     """pkv_paged_decode_attention with the library's fixed scratch instead of a workspace.
@@ -247,7 +274,7 @@ def alloc_workspace(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, devic
     """A device buffer of pkv_decode_workspace_bytes (allocated by torch; None when 0)."""
     t = _torch()
     n = pkv_decode_workspace_bytes(desc, n_seqs, max_blocks_per_seq)
-    return t.empty(max(n, 16) // 4 + 4, dtype=t.float32, device=device) if n else None
+    return t.zeros(max(n, 16) // 4 + 4, dtype=t.float32, device=device) if n else None
 
 
 # ---- host block manager -------------------------------------------------------------------------

@@ -60,11 +60,11 @@ def test_validate_desc(kw, want):
 
 def test_workspace_only_when_split():
     d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)
-    assert pkv.pkv_decode_workspace_bytes(d, 64, 32) == 0          # one partition per sequence
-    n = pkv.pkv_decode_workspace_bytes(d, 64, 129)                 # 129 blocks -> 5 partitions of 32
-    assert n == 64 * 32 * 5 * (128 + 2) * 4
+    assert pkv.pkv_decode_workspace_bytes(d, 64, 64) == 0          # one partition per sequence
+    n = pkv.pkv_decode_workspace_bytes(d, 64, 129)
+    assert n == 64 * 32 * 3 * (128 + 2) * 4 + 64 * 32 * 8          # 129 blocks -> 3 partitions of 64
     d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)
-    assert pkv.pkv_decode_workspace_bytes(d4, 10, 2048) == 10 * 16 * 64 * (256 + 2) * 4
+    assert pkv.pkv_decode_workspace_bytes(d4, 10, 2048) == 10 * 16 * 32 * (256 + 2) * 4 + 10 * 4 * 8
     assert pkv.pkv_decode_workspace_bytes(d, 0, 10) == 0
 
 

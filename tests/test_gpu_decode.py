@@ -150,3 +150,87 @@ def test_bad_table_entry_and_length_are_flagged_not_read():
     _, flags = run_decode("f16", q, kp, vp, tables, lens2, 0.125, 2, 2, 64)
     assert flags & pkv.PKV_DEV_BAD_CONTEXT_LEN
     assert pkv.pkv_get_device_status() == 0            # reading clears the word
+
+
+@pytest.mark.parametrize("dtype,n_q,n_kv,d", [("f16", 8, 8, 128), ("bf16", 16, 4, 256), ("f32", 4, 2, 64),
+                                              ("f16", 4, 1, 64)])
+def test_fused_append_equals_separate_calls(dtype, n_q, n_kv, d):
+    """pkv_paged_decode_append_attention == pkv_kv_append(slot of position len-1) + decode, bit for bit."""
+    import torch
+    lens = [1, 16, 17, 40, 513, 1500, 0]
+    q, kp, vp, tables, lens_a, nb = paged_case(dtype, lens, n_q, n_kv, d, seed=41, n_layers=2)
+    rng = np.random.default_rng(42)
+    kn = W.normal_values(rng, (len(lens), n_kv, d), dtype)
+    vn = W.normal_values(rng, (len(lens), n_kv, d), dtype)
+    desc = pkv.make_desc(dtype, 2, nb, n_q, n_kv, d)
+    t_t = torch.from_numpy(tables).cuda()
+    l_t = torch.from_numpy(lens_a).cuda()
+    ws = pkv.alloc_workspace(desc, len(lens), tables.shape[1])
+    # separate calls: append at the slot of the last position (padding for empty sequences)
+    slots = np.array([tables[s, (n - 1) // 16] * 16 + (n - 1) % 16 if n > 0 else -1 for s, n in enumerate(lens_a)],
+                     dtype=np.int64)
+    k1, v1 = to_torch(kp, dtype), to_torch(vp, dtype)
+    out1 = torch.full_like(to_torch(q, dtype), float("nan"))
+    pkv.pkv_kv_append(desc, 1, to_torch(kn, dtype), to_torch(vn, dtype), torch.from_numpy(slots).cuda(), k1, v1)
+    pkv.pkv_paged_decode_attention(desc, 1, to_torch(q, dtype), k1, v1, t_t, l_t, 0.1, out1, ws)
+    k2, v2 = to_torch(kp, dtype), to_torch(vp, dtype)
+    out2 = torch.full_like(out1, float("nan"))
+    pkv.pkv_paged_decode_append_attention(desc, 1, to_torch(q, dtype), to_torch(kn, dtype), to_torch(vn, dtype),
+                                          k2, v2, t_t, l_t, 0.1, out2, ws)
+    assert pkv.pkv_get_device_status() == 0
+    for a_, b_ in ((k1, k2), (v1, v2)):
+        assert torch.equal(a_.contiguous().view(torch.uint8), b_.contiguous().view(torch.uint8))
+    assert torch.equal(out1.contiguous().view(torch.uint8), out2.contiguous().view(torch.uint8))
+    # and against the oracle, whose pools receive the same rows at the same slots
+    want_k, want_v = kp.copy(), vp.copy()
+    oracle.kv_append(kn, vn, slots, want_k[1], want_v[1])
+    want = oracle.paged_decode(dtype, q, want_k[1], want_v[1], tables, lens_a, 0.1)
+    got = as_f64(out2)
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
+
+
+def test_workspace_garbage_and_reuse_across_shapes():
+    """Split-K arrival counters self-initialise: a garbage-filled workspace, reused by calls of
+    different shapes (whose counters land on each other's partials), gives correct rows."""
+    import torch
+    ws = torch.randint(-2 ** 31, 2 ** 31 - 1, (4 << 20,), dtype=torch.int32, device="cuda")
+    for dtype, lens, n_q, n_kv, d, seed in (("f16", [700, 1500, 33], 8, 2, 128, 51),
+                                            ("bf16", [2100, 5, 900, 64, 1200], 4, 4, 64, 52),
+                                            ("f32", [1000, 17], 2, 1, 256, 53),
+                                            ("f16", [700, 1500, 33], 8, 2, 128, 54)):
+        q, kp, vp, tables, lens_a, nb = paged_case(dtype, lens, n_q, n_kv, d, seed)
+        desc = pkv.make_desc(dtype, 1, nb, n_q, n_kv, d)
+        assert pkv.pkv_decode_workspace_bytes(desc, len(lens), tables.shape[1]) > 0
+        out = torch.full_like(to_torch(q, dtype), float("nan"))
+        pkv.pkv_paged_decode_attention(desc, 0, to_torch(q, dtype), to_torch(kp, dtype), to_torch(vp, dtype),
+                                       torch.from_numpy(tables).cuda(), torch.from_numpy(lens_a).cuda(), 0.1, out,
+                                       ws)
+        assert pkv.pkv_get_device_status() == 0
+        want = oracle.paged_decode(dtype, q, kp[0], vp[0], tables, lens_a, 0.1)
+        assert np.max(np.abs(as_f64(out) - want)) <= TOL[dtype]
+
+
+def test_cuda_graph_replay_of_split_decode():
+    """A captured decode launch replays with the same call tag; the merging CTA's counter reset
+    keeps every replay correct."""
+    import torch
+    dtype, n_q, n_kv, d = "bf16", 8, 2, 128
+    q, kp, vp, tables, lens, nb = paged_case(dtype, [1500, 3000, 70], n_q, n_kv, d, seed=55)
+    desc = pkv.make_desc(dtype, 1, nb, n_q, n_kv, d)
+    args = [to_torch(q, dtype), to_torch(kp, dtype), to_torch(vp, dtype), torch.from_numpy(tables).cuda(),
+            torch.from_numpy(lens).cuda()]
+    ws = pkv.alloc_workspace(desc, 3, tables.shape[1])
+    eager = torch.empty_like(args[0])
+    pkv.pkv_paged_decode_attention(desc, 0, args[0], args[1], args[2], args[3], args[4], 0.1, eager, ws)
+    out = torch.zeros_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pkv.pkv_paged_decode_attention(desc, 0, args[0], args[1], args[2], args[3], args[4], 0.1, out, ws)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pkv.pkv_get_device_status() == 0

@@ -21,8 +21,9 @@ from paged_kv_cache_258_gb300.engine import DecodeBatch, PagedKVCache
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("dtype,n_q,n_kv,d", [("f16", 4, 4, 64), ("bf16", 8, 2, 128), ("f32", 4, 1, 64)])
-def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d):
+def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d, fused):
     rng = np.random.default_rng(77)
     L, n_groups, n_members, n_steps = 2, 3, 12, 24
     prompts = [int(100 + rng.integers(1, 16)) for _ in range(n_groups)]   # partial shared tails
@@ -49,7 +50,7 @@ def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d):
         cache.fork(roots[m % n_groups], m)
         assert mo.fork(roots[m % n_groups], m) == "ok"
         live.append(m)
-    batch = DecodeBatch(cache, live, max_blocks=(max(prompts) + n_steps + 32) // 16 + 1)
+    batch = DecodeBatch(cache, live, max_blocks=(max(prompts) + n_steps + 32) // 16 + 1, fused=fused)
     next_id = n_members
     scale = 1.0 / np.sqrt(d)
     cow_seen = 0
