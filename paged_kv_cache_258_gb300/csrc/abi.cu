@@ -62,7 +62,7 @@ namespace pkv {
 // launch agree on every device.
 int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
     const long long target = 4LL * 152;
-    int bpp = 64;
+    int bpp = kMaxBpp;
     while (bpp > 4 && (long long)n_seqs * n_kv * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
     return bpp;
 }

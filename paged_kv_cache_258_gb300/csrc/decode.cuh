@@ -74,7 +74,8 @@ struct DecodeSmem {
     static constexpr size_t STAGES = (size_t)NW * ST * 2 * Geo::CHUNK * sizeof(T);
     static constexpr size_t BARS = STAGES;                                 // uint64 [NW][ST]
     static constexpr size_t PHYS = BARS + (size_t)NW * ST * 8;             // int [NW][ST]
-    static constexpr size_t ZBUF = (PHYS + (size_t)NW * ST * 4 + 15) / 16 * 16;  // float [NW][G*16]
+    static constexpr size_t TAB = PHYS + (size_t)NW * ST * 4;              // int [NW][kMaxBpp/NW]: block ids
+    static constexpr size_t ZBUF = (TAB + (size_t)kMaxBpp * 4 + 15) / 16 * 16;  // float [NW][G*16]
     static constexpr size_t PBUF = ZBUF + (size_t)NW * G * kBlock * 4;    // float [NW][G*16]
     static constexpr size_t ML = PBUF + (size_t)NW * G * kBlock * 4;      // float [NW][G][2]
     static constexpr size_t TOTAL = ML + (size_t)NW * G * 2 * 4;
@@ -260,6 +261,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
     float* s_p = s_pall + warp * G * kBlock;
 
     const int32_t* trow = a.tables + (size_t)s * a.max_blocks + b0;
+    static_assert(kMaxBpp % NW == 0, "each warp stages kMaxBpp / NW table entries");
+    int* wtab = reinterpret_cast<int*>(smem + S::TAB) + warp * (kMaxBpp / NW);
     const T* kbase = reinterpret_cast<const T*>(a.k_layer);
     const T* vbase = reinterpret_cast<const T*>(a.v_layer);
     const int nk = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;  // blocks of this warp
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
     // lane 0: start the copies of this warp's k-th block into stage k % ST
     auto issue = [&](int k) {
         const int st = k % ST;
-        const int phys = trow[warp + k * NW];
+        const int phys = wtab[k];
         const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
         wphys[st] = ok ? phys : -1;
         if (ok) {
@@ -282,6 +285,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
             mbar_arrive(&wbars[st]);  // completes the phase with nothing copied: rows are masked
         }
     };
+    // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
+    // waits on a global read of the table
+    for (int k = lane; k < nk; k += 32) wtab[k] = trow[warp + k * NW];
+    __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < ST && k < nk; ++k) issue(k);
     }

@@ -112,7 +112,8 @@ struct MmaSmem {
     static constexpr size_t STAGES = (size_t)NW * ST * 2 * TILE;     // 1024-aligned base
     static constexpr size_t BARS = STAGES;                           // uint64 [NW][ST]
     static constexpr size_t PHYS = BARS + (size_t)NW * ST * 8;      // int [NW][ST]
-    static constexpr size_t ML = (PHYS + (size_t)NW * ST * 4 + 15) / 16 * 16;  // float [NW][8][2]
+    static constexpr size_t TAB = PHYS + (size_t)NW * ST * 4;       // int [NW][kMaxBpp/NW]: block ids
+    static constexpr size_t ML = (TAB + (size_t)kMaxBpp * 4 + 15) / 16 * 16;  // float [NW][8][2]
     static constexpr size_t TOTAL = ML + (size_t)NW * 8 * 2 * 4;
     static constexpr size_t ALLOC = TOTAL + 1024;                     // room to align the base
     static constexpr size_t MERGE = (size_t)NW * 8 * D * 4;          // merge scratch, after the combine buffer
@@ -173,12 +174,14 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const uint32_t wstage = smem_addr(smem) + (uint32_t)(warp * ST) * 2 * TILE;
     unsigned char* wstage_ptr = smem + (size_t)warp * ST * 2 * TILE;
     const int32_t* trow = a.tables + (size_t)s * a.max_blocks + b0;
+    static_assert(kMaxBpp % NW == 0, "each warp stages kMaxBpp / NW table entries");
+    int* wtab = reinterpret_cast<int*>(smem + S::TAB) + warp * (kMaxBpp / NW);
     const int nk = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const uint64_t policy = l2_evict_first_policy();
 
     auto issue = [&](int k) {  // lane 0 only
         const int st = k % ST;
-        const int phys = trow[warp + k * NW];
+        const int phys = wtab[k];
         const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
         wphys[st] = ok ? phys : -1;
         if (ok) {
@@ -195,6 +198,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
             mbar_arrive(&wbars[st]);
         }
     };
+    // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
+    // waits on a global read of the table
+    for (int k = lane; k < nk; k += 32) wtab[k] = trow[warp + k * NW];
+    __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < ST && k < nk; ++k) issue(k);
     }

@@ -11,6 +11,7 @@
 namespace pkv {
 
 constexpr int kBlock = 16;  // tokens per block; the only block size compiled
+constexpr int kMaxBpp = 64; // largest partition (table entries per CTA); decode kernels stage them in smem
 
 // Arguments of one paged decode attention launch (one layer). Pointers are device pointers
 // already offset to the layer; element types are fixed by the template instantiation.
