@@ -110,8 +110,8 @@ template <int D, int NW, int ST>
 struct MmaSmem {
     static constexpr size_t TILE = 16 * D * 2;                       // one K or V tile (bytes)
     static constexpr size_t STAGES = (size_t)NW * ST * 2 * TILE;     // 1024-aligned base
-    static constexpr size_t BARS = STAGES;                           // uint64 [NW][ST]
-    static constexpr size_t PHYS = BARS + (size_t)NW * ST * 8;      // int [NW][ST]
+    static constexpr size_t BARS = STAGES;                           // uint64 [NW][ST][K, V]
+    static constexpr size_t PHYS = BARS + (size_t)NW * ST * 16;     // int [NW][ST]
     static constexpr size_t TAB = PHYS + (size_t)NW * ST * 4;       // int [NW][kMaxBpp/NW]: block ids
     static constexpr size_t ML = (TAB + (size_t)kMaxBpp * 4 + 15) / 16 * 16;  // float [NW][8][2]
     static constexpr size_t TOTAL = ML + (size_t)NW * 8 * 2 * 4;
@@ -165,11 +165,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const bool single = nb <= a.bpp;
     fused_append<T, D, NW * 32>(a, s, g, p, ctx, nb);
 
-    if (threadIdx.x < NW * ST) mbar_init(&bars[threadIdx.x], 1);
+    // Two mbarriers per stage: K tile (even) and V tile (odd), so QK^T starts as soon as K lands and
+    // the next K copy is issued before PV runs.
+    if (threadIdx.x < 2 * NW * ST) mbar_init(&bars[threadIdx.x], 1);
     fence_mbar_init();
     __syncthreads();
 
-    uint64_t* wbars = bars + warp * ST;
+    uint64_t* wbars = bars + warp * ST * 2;  // [ST][K, V]
     int* wphys = s_phys + warp * ST;
     const uint32_t wstage = smem_addr(smem) + (uint32_t)(warp * ST) * 2 * TILE;
     unsigned char* wstage_ptr = smem + (size_t)warp * ST * 2 * TILE;
@@ -179,31 +181,37 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const int nk = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const uint64_t policy = l2_evict_first_policy();
 
-    auto issue = [&](int k) {  // lane 0 only
+    // lane 0: start the copy of the K (v = 0) or V (v = 1) tile of this warp's k-th block
+    auto issue = [&](int k, int v) {
         const int st = k % ST;
         const int phys = wtab[k];
         const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
-        wphys[st] = ok ? phys : -1;
+        uint64_t* bar = &wbars[st * 2 + v];
+        if (v == 0) wphys[st] = ok ? phys : -1;
         if (ok) {
             const int row0 = (phys * a.n_kv + g) * kBlock;
-            const uint32_t dst = wstage + (uint32_t)st * 2 * TILE;
-            mbar_arrive_expect_tx(&wbars[st], 2 * TILE);
+            const uint32_t dst = wstage + (uint32_t)st * 2 * TILE + (uint32_t)v * TILE;
+            mbar_arrive_expect_tx(bar, TILE);
 #pragma unroll
-            for (int pn = 0; pn < PANELS; ++pn) {
-                tma_load_2d(dst + pn * 2048, &tm_k, pn * 64, row0, &wbars[st], policy);
-                tma_load_2d(dst + TILE + pn * 2048, &tm_v, pn * 64, row0, &wbars[st], policy);
-            }
+            for (int pn = 0; pn < PANELS; ++pn) tma_load_2d(dst + pn * 2048, v ? &tm_v : &tm_k, pn * 64, row0, bar, policy);
         } else {
-            atomicOr(a.status, (unsigned)PKV_DEV_BAD_BLOCK_ID);
-            mbar_arrive(&wbars[st]);
+            if (v == 0) atomicOr(a.status, (unsigned)PKV_DEV_BAD_BLOCK_ID);
+            mbar_arrive(bar);  // completes the phase with nothing copied: the block is masked
         }
+    };
+    // after a timed-out wait: wait (bounded) for the tiles of blocks [k0, k1) of kind v still in flight
+    auto drain = [&](int k0, int k1, int v) {
+        for (int kk = k0; kk < k1 && kk < nk; ++kk) mbar_wait_bounded(&wbars[(kk % ST) * 2 + v], (uint32_t)(kk / ST) & 1u);
     };
     // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
     // waits on a global read of the table
     for (int k = lane; k < nk; k += 32) wtab[k] = trow[warp + k * NW];
     __syncwarp();
     if (lane == 0) {
-        for (int k = 0; k < ST && k < nk; ++k) issue(k);
+        for (int k = 0; k < ST && k < nk; ++k) {
+            issue(k, 0);
+            issue(k, 1);
+        }
     }
 
     // Q^T fragments (B operand of S = K Q^T): row gid, dims 16ks + 2tig (+1) and +8; rows >= G are 0.
@@ -239,27 +247,19 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
 
     for (int k = 0; k < nk; ++k) {
         const int st = k % ST;
-        if (!mbar_wait_bounded(&wbars[st], (uint32_t)(k / ST) & 1u)) {
+        const uint32_t par = (uint32_t)(k / ST) & 1u;
+        if (!mbar_wait_bounded(&wbars[st * 2], par)) {
             if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
-            for (int kk = k + 1; kk < k + ST && kk < nk; ++kk)
-                mbar_wait_bounded(&wbars[kk % ST], (uint32_t)(kk / ST) & 1u);
+            drain(k, k + ST, 0);  // K tiles of blocks k .. k+ST-1 may be in flight
+            drain(k, k + ST, 1);  // and their V tiles
             break;
         }
         const int jb = (b0 + warp + k * NW) * kBlock;
         const int nvalid = wphys[st] >= 0 ? min(kBlock, ctx - jb) : 0;
         const uint32_t sK = wstage + (uint32_t)st * 2 * TILE;
         const uint32_t sV = sK + TILE;
+        uint32_t b0f = 0u, b1f = 0u;
         if (nvalid > 0) {
-            if (nvalid < kBlock) {  // zero the V rows past the context (they may hold anything)
-                unsigned char* vt = wstage_ptr + (size_t)st * 2 * TILE + TILE;
-                const int nch = (kBlock - nvalid) * (D / 8);
-                for (int i = lane; i < nch; i += 32) {
-                    const int r = nvalid + i / (D / 8);
-                    const int ch = i % (D / 8);
-                    *reinterpret_cast<uint4*>(vt + swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
-            }
             // ---- S = K Q^T (16 tokens x 8 rows), fp32 ----
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
             const float2 ra = M::unpack(pa), rb = M::unpack(pb);  // the rounded weights the MMA uses
             l_run[0] = l_run[0] * al0 + ra.x + rb.x;
             l_run[1] = l_run[1] * al1 + ra.y + rb.y;
-            const uint32_t b0f = movmatrix_trans(pa);  // P^T: tokens 2tig, 2tig+1 of row gid
-            const uint32_t b1f = movmatrix_trans(pb);  // tokens 8+2tig, 9+2tig of row gid
+            b0f = movmatrix_trans(pa);  // P^T: tokens 2tig, 2tig+1 of row gid
+            b1f = movmatrix_trans(pb);  // tokens 8+2tig, 9+2tig of row gid
             if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
@@ -305,6 +305,29 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
                     acc[mt][3] *= al1;
                 }
             }
+        }
+        __syncwarp();  // the K tile has been read by every lane
+        if (lane == 0 && k + ST < nk) {
+            fence_proxy_async_smem();
+            issue(k + ST, 0);
+        }
+        if (!mbar_wait_bounded(&wbars[st * 2 + 1], par)) {
+            if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
+            drain(k + 1, k + ST + 1, 0);  // K tiles of blocks k+1 .. k+ST may be in flight
+            drain(k, k + ST, 1);          // V tiles of blocks k .. k+ST-1
+            break;
+        }
+        if (nvalid > 0) {
+            if (nvalid < kBlock) {  // zero the V rows past the context (they may hold anything)
+                unsigned char* vt = wstage_ptr + (size_t)st * 2 * TILE + TILE;
+                const int nch = (kBlock - nvalid) * (D / 8);
+                for (int i = lane; i < nch; i += 32) {
+                    const int r = nvalid + i / (D / 8);
+                    const int ch = i % (D / 8);
+                    *reinterpret_cast<uint4*>(vt + swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
             // ---- O^T += V^T P^T (16 dims x 8 rows per instruction) ----
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) {
@@ -313,10 +336,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
                 M::mma(acc[mt], af, b0f, b1f);
             }
         }
-        __syncwarp();
+        __syncwarp();  // the V tile has been read by every lane
         if (lane == 0 && k + ST < nk) {
             fence_proxy_async_smem();
-            issue(k + ST);
+            issue(k + ST, 1);
         }
     }
 

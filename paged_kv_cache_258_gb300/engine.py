@@ -7,8 +7,9 @@ method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAtten
 
   1. host:   the block manager reserves one slot per sequence (taking a fresh block or
              copying a shared tail on write) and packs the block tables;
-  2. H2D:    slots, tables, lengths and copy pairs go to device buffers (pinned staging,
-             double-buffered so the host can plan step i+1 while step i's copy is pending);
+  2. H2D:    slots, tables, lengths and copy pairs go to the device in one copy (one pinned
+             image per step, double-buffered so the host can plan step i+1 while step i's copy is
+             pending);
   3. device: copy-on-write block copies, then per layer the KV append and the paged decode
              attention -- copies before appends (else a copy would overwrite the new row),
              appends before attention (the new token attends to itself). By default the append
@@ -77,29 +78,35 @@ class DecodeBatch:
         self.fused = bool(fused)
         dev = cache.device
         n, mb = self.n, self.max_blocks
-        # device metadata (fixed addresses: the launches see the same pointers every step)
-        self.d_slots = torch.empty(n, dtype=torch.int64, device=dev)
-        self.d_tables = torch.empty((n, mb), dtype=torch.int32, device=dev)
-        self.d_lens = torch.empty(n, dtype=torch.int32, device=dev)
-        self.d_pairs = torch.empty((max(n, 1), 2), dtype=torch.int32, device=dev)
+        # One int32 metadata image per step, [slots (int64) | tables | lens | CoW pairs], so the
+        # upload is a single copy; the device copy has fixed addresses across steps.
+        self._o_tab = 2 * n
+        self._o_len = self._o_tab + n * mb
+        self._o_pair = self._o_len + n
+        self._meta_words = self._o_pair + 2 * max(n, 1)
+        d_meta = torch.empty(self._meta_words, dtype=torch.int32, device=dev)
+        self.d_meta = d_meta
+        self.d_slots, self.d_tables, self.d_lens, self.d_pairs = self._views(d_meta)
         self.workspace = pkv.alloc_workspace(cache.desc, n, mb, device=dev)
-        # two pinned staging sets
+        # two pinned staging images
         self._stage = []
         for _ in range(2):
-            self._stage.append(dict(
-                slots=torch.empty(n, dtype=torch.int64).pin_memory(),
-                tables=torch.empty((n, mb), dtype=torch.int32).pin_memory(),
-                lens=torch.empty(n, dtype=torch.int32).pin_memory(),
-                pairs=torch.empty((max(n, 1), 2), dtype=torch.int32).pin_memory(),
-                done=torch.cuda.Event(),
-                used=False,
-            ))
+            h_meta = torch.empty(self._meta_words, dtype=torch.int32).pin_memory()
+            slots, tables, lens, pairs = self._views(h_meta)
+            self._stage.append(dict(meta=h_meta, slots=slots, tables=tables, lens=lens, pairs=pairs,
+                                    done=torch.cuda.Event(), used=False))
         self._turn = 0
         self.last_lens = np.zeros(n, dtype=np.int32)
         self.last_n_pairs = 0
         self.total_cow = 0
         self.manager_s = 0.0       # host time in the block manager (append + pack), waits excluded
         self.steps_planned = 0
+
+    def _views(self, buf):
+        n, mb = self.n, self.max_blocks
+        import torch
+        return (buf[: 2 * n].view(torch.int64), buf[self._o_tab: self._o_len].view(n, mb),
+                buf[self._o_len: self._o_pair], buf[self._o_pair:].view(-1, 2))
 
     def set_sequences(self, seq_ids) -> None:
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
@@ -134,12 +141,9 @@ class DecodeBatch:
 
     def upload(self, st: dict) -> None:
         import torch
+        words = self._o_pair + 2 * st["npairs"]  # only the pairs this step emitted
         with torch.cuda.stream(self.stream):
-            self.d_slots.copy_(st["slots"], non_blocking=True)
-            self.d_tables.copy_(st["tables"], non_blocking=True)
-            self.d_lens.copy_(st["lens"], non_blocking=True)
-            if st["npairs"]:
-                self.d_pairs[: st["npairs"]].copy_(st["pairs"][: st["npairs"]], non_blocking=True)
+            self.d_meta[:words].copy_(st["meta"][:words], non_blocking=True)
             st["done"].record(self.stream)
         st["used"] = True
 
