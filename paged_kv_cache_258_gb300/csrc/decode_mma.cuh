@@ -146,6 +146,15 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const int g = blockIdx.y;
     const int s = blockIdx.z;
 
+    // This warp's table entries of the partition (blocks p*bpp + warp + k*NW, k < kMaxBpp/NW <= 32),
+    // loaded before the context length is known so the two global reads overlap; entries past the
+    // sequence's last block are read (inside the table row) but never used.
+    static_assert(kMaxBpp / NW <= 32, "one table entry per lane");
+    int tab_pre = -1;
+    {
+        const int idx = p * a.bpp + warp + lane * NW;
+        if (lane < kMaxBpp / NW && idx < a.max_blocks) tab_pre = a.tables[(size_t)s * a.max_blocks + idx];
+    }
     int ctx = a.lens[s];
     const int cap = a.max_blocks * kBlock;
     if (ctx < 0 || ctx > cap) {
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     };
     // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
     // waits on a global read of the table
-    for (int k = lane; k < nk; k += 32) wtab[k] = trow[warp + k * NW];
+    if (lane < nk) wtab[lane] = tab_pre;
+    (void)trow;
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < ST && k < nk; ++k) {

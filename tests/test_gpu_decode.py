@@ -234,3 +234,12 @@ def test_cuda_graph_replay_of_split_decode():
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert pkv.pkv_get_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,n_q,n_kv,d", [("f16", 4, 2, 64), ("bf16", 8, 1, 128)])
+def test_large_batch(dtype, n_q, n_kv, d):
+    """1,100 sequences of mostly short contexts (many idle partitions), split-K included."""
+    rng = np.random.default_rng(61)
+    lens = rng.integers(0, 90, size=1100)
+    lens[:8] = (1, 16, 17, 300, 700, 1100, 0, 64)
+    check(dtype, lens, n_q, n_kv, d, seed=61)
