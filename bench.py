@@ -185,14 +185,18 @@ def _build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
     return wl, desc, None
 
 
-def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int = 0, layers: int | None = None):
+def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int = 0, layers: int | None = None,
+                   placement: str = "shuffled"):
     import torch
     from paged_kv_cache_258_gb300 import pkv
     from paged_kv_cache_258_gb300.engine import DecodeBatch, PagedKVCache
 
     wl, wdesc, churn = build_workload(name, warmup, steps, seed_offset, layers)
     desc = pkv.make_desc(wl.dtype, wl.n_layers, wl.num_blocks, wl.n_q_heads, wl.n_kv_heads, wl.head_dim)
-    cache = PagedKVCache(desc, free_order=W.free_order(wl.num_blocks, wl.seed), device=device, init="randn",
+    # shuffled: the free list is a seeded permutation, so a sequence's blocks lie anywhere in the pool;
+    # contiguous: blocks are handed out in id order, so each sequence's blocks are adjacent
+    order = W.free_order(wl.num_blocks, wl.seed) if placement == "shuffled" else None
+    cache = PagedKVCache(desc, free_order=order, device=device, init="randn",
                          seed=wl.seed)
     extra = warmup + 2 * steps + 2 * W.BLOCK
     if churn is None:
@@ -249,7 +253,8 @@ def run_gpu(args) -> dict | None:
     device = torch.device("cuda", local)
     pkv.lib()
     wl, wdesc, cache, batch, (q, k_new, v_new, out), state = setup_gpu_case(
-        args.config, args.warmup, args.steps, device, seed_offset=rank, layers=args.layers)
+        args.config, args.warmup, args.steps, device, seed_offset=rank, layers=args.layers,
+        placement=args.placement)
     stream = batch.stream
     scale = wl.scale
 
@@ -345,13 +350,14 @@ def run_gpu(args) -> dict | None:
             "kv_gib_per_step": round(kv_bytes / args.steps / 2 ** 30, 3),
             "l2": "no flush: every step reads more KV than the 129 MB L2 holds",
             "parallelism": f"replicas x{ws} (sequences shard by rank, no collective)",
+            "placement": args.placement,
         },
         "tokens_per_s": round(total_seqs / (elapsed_ms * 1e-3), 1),
         "hbm_frac_of_measured": round(value / hbm_peak, 4),
         "hbm_frac_of_nominal_7900": round(value / NOMINAL_HBM_GBS, 4),
         "roofline": {
             "kernel": ("paged_decode_mma_kernel" if wl.dtype != "f32" else "paged_decode_kernel")
-                      + " (+ splitk_combine_kernel when a sequence has several partitions)",
+                      + " (split-K partitions merged inside the same launch)",
             "bound": "hbm",
             "achieved": round(achieved_gbs, 2),
             "peak": hbm_peak,
@@ -529,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
+    ap.add_argument("--placement", default="shuffled", choices=["shuffled", "contiguous"],
+                    help="physical placement of each sequence's blocks (indirection-overhead study)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:

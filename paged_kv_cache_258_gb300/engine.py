@@ -19,6 +19,7 @@ All device work is in libpkv's kernels; this module only moves arguments.
 """
 from __future__ import annotations
 
+import ctypes
 import time
 
 import numpy as np
@@ -71,6 +72,7 @@ class DecodeBatch:
         import torch
         self.cache = cache
         self.seq_ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        self._p_ids = self.seq_ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
         self.n = len(self.seq_ids)
         self.max_blocks = int(max_blocks)
         self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
@@ -93,7 +95,15 @@ class DecodeBatch:
         for _ in range(2):
             h_meta = torch.empty(self._meta_words, dtype=torch.int32).pin_memory()
             slots, tables, lens, pairs = self._views(h_meta)
+            # numpy views of the pinned image and ctypes pointers into it, made once: planning a step
+            # is two C calls writing straight into the staging image
+            np_lens = lens.numpy()
             self._stage.append(dict(meta=h_meta, slots=slots, tables=tables, lens=lens, pairs=pairs,
+                                    np_lens=np_lens,
+                                    p_slots=slots.numpy().ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                    p_pairs=pairs.numpy().ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                    p_tables=tables.numpy().ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                    p_lens=np_lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                     done=torch.cuda.Event(), used=False))
         self._turn = 0
         self.last_lens = np.zeros(n, dtype=np.int32)
@@ -113,6 +123,7 @@ class DecodeBatch:
         if len(ids) != self.n:
             raise ValueError("batch size is fixed")
         self.seq_ids = ids
+        self._p_ids = ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
 
     def plan(self) -> dict:
         """Host part of a step: reserve slots, collect CoW pairs, pack tables (pinned)."""
@@ -121,20 +132,21 @@ class DecodeBatch:
         if st["used"]:
             st["done"].synchronize()  # the GPU has consumed this staging set
         t0 = time.perf_counter()
-        rc, slots, pairs, n_done = self.cache.mgr.append_batch(self.seq_ids)
+        L = pkv.lib()
+        h = self.cache.mgr._h
+        n_cow, n_done = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = L.pkv_mgr_append_batch(h, self._p_ids, self.n, st["p_slots"], st["p_pairs"], ctypes.byref(n_cow),
+                                    ctypes.byref(n_done))
         if rc != pkv.PKV_OK:
-            raise pkv.PkvError(rc, f"append_batch stopped at sequence {int(self.seq_ids[n_done])}")
-        st["slots"].numpy()[:] = slots
-        npairs = len(pairs)
-        if npairs:
-            st["pairs"].numpy()[:npairs] = pairs
-        rc, _, _ = self.cache.mgr.pack_tables(self.seq_ids, self.max_blocks, st["tables"].numpy(), st["lens"].numpy())
+            raise pkv.PkvError(rc, f"append_batch stopped at sequence {int(self.seq_ids[n_done.value])}")
+        npairs = int(n_cow.value)
+        rc = L.pkv_mgr_pack_tables(h, self._p_ids, self.n, self.max_blocks, st["p_tables"], st["p_lens"])
         if rc != pkv.PKV_OK:
             raise pkv.PkvError(rc, "pack_tables (is max_blocks wide enough?)")
         st["npairs"] = npairs
         self.manager_s += time.perf_counter() - t0
         self.steps_planned += 1
-        self.last_lens = st["lens"].numpy().copy()
+        self.last_lens = st["np_lens"].copy()
         self.last_n_pairs = npairs
         self.total_cow += npairs
         return st
