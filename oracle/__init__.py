@@ -1,8 +1,8 @@
 """Oracle package -- TEST INFRASTRUCTURE, not part of the product.
 
 Plain, slow, obviously correct CPU statements of the paged KV cache hot path:
-  * ``oracle.c`` (fp64 C): paged decode attention, KV append, copy-on-write block copy,
-    KV bytes per token, and its own fp16 / bf16 decoders;
+  * ``oracle.c`` (fp64 C): paged decode attention, paged (chunked) prefill attention, KV
+    append, copy-on-write block copy, KV bytes per token, and its own fp16 / bf16 decoders;
   * ``manager.py`` (Python): the block manager (free list, block tables, refcounts,
     prefix sharing, copy-on-write, admission in blocks).
 
@@ -58,6 +58,11 @@ def lib():
             vp, vp, vp, i32p, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_double,
             ctypes.POINTER(ctypes.c_double), ctypes.c_int]
         L.oracle_paged_decode.restype = ctypes.c_int
+        L.oracle_paged_prefill.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            vp, vp, vp, i32p, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.POINTER(ctypes.c_double), ctypes.c_int]
+        L.oracle_paged_prefill.restype = ctypes.c_int
         L.oracle_kv_append.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             vp, vp, i64p, ctypes.c_int, vp, vp]
@@ -126,6 +131,35 @@ def paged_decode(dtype, q, k_pool, v_pool, tables, lens, scale, n_threads: int =
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
     if rc != 0:
         raise ValueError("oracle_paged_decode refused its arguments")
+    return out
+
+
+def paged_prefill(dtype, q, k_pool, v_pool, tables, lens, query_start, scale, n_threads: int = 1) -> np.ndarray:
+    """fp64 paged prefill attention for one layer (causal chunk of new tokens per sequence).
+
+    q [n_tokens, n_q, d]; pools, tables and lens as paged_decode; query_start [n_seqs + 1]:
+    the tokens of sequence s are q rows query_start[s] .. query_start[s+1]-1, at positions
+    lens[s] - n_s .. lens[s] - 1. Returns float64 [n_tokens, n_q, d] (rows of no sequence: 0).
+    """
+    code = _code(dtype)
+    eb = elem_bytes(code)
+    q, k_pool, v_pool = _raw(q, eb), _raw(k_pool, eb), _raw(v_pool, eb)
+    tables, lens, query_start = _i32(tables), _i32(lens), _i32(query_start)
+    n_tokens, n_q, d = q.shape
+    num_blocks, n_kv, bs, d2 = k_pool.shape
+    n_seqs = lens.shape[0]
+    assert d2 == d and v_pool.shape == k_pool.shape
+    if tables.ndim != 2 or tables.shape[0] != n_seqs or query_start.shape != (n_seqs + 1,):
+        raise ValueError("tables / lens / query_start shape mismatch")
+    out = np.zeros((n_tokens, n_q, d), dtype=np.float64)
+    rc = lib().oracle_paged_prefill(
+        code, n_q, n_kv, d, bs, num_blocks, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+        tables.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), tables.shape[1],
+        lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        query_start.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n_seqs, n_tokens, float(scale),
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_paged_prefill refused its arguments")
     return out
 
 

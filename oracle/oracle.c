@@ -11,7 +11,8 @@
  *      step 1  the KV cache is cut into fixed blocks of B_block tokens;
  *      step 2  a per-sequence block table maps logical block i to physical block X;
  *      step 3  appending a token writes into the last block (slot = X*B_block + offset);
- *      step 5  attention takes the block table and gathers the rows itself.
+ *      step 5  attention takes the block table and gathers the rows itself (decode: one
+ *              query per sequence; prefill: a chunk of causal queries per sequence).
  *    Section "Lo que deberias llevarte", item 2: paging changes the memory layout only, so
  *    the result is exactly dense softmax attention over the gathered rows.
  *  - "PagedAttention e continuous batching", section "01 - Conceito", paragraph 6:
@@ -194,6 +195,102 @@ int oracle_paged_decode(int dtype, int n_q, int n_kv, int head_dim, int block_si
             double acc = 0.0;
             for (int j = 0; j < n; ++j) acc += (z[j] / zsum) * vc[(size_t)j * head_dim + i];
             o[i] = acc;
+        }
+        free(kc); free(vc); free(qv); free(z);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Paged prefill attention for one layer: a chunk of several new query tokens per sequence,
+ * each attending causally to the sequence's cache through its block table.
+ * "PagedAttention e continuous batching", section "01 - Conceito", paragraph 5 slices a long
+ * prompt into chunks that share steps with decoding; "La idea de PagedAttention", step 5, has
+ * the kernel gather the rows through the table. Reading taken (the pages give no formula for
+ * the chunk): the n_s tokens of sequence s's chunk are its newest, already appended, so with
+ * c = lens[s] they sit at positions c - n_s .. c - 1, and the token at position p attends to
+ * positions 0 .. p (causal), exactly as dense causal attention over the gathered rows.
+ *   q            [n_tokens][n_q][head_dim] (dtype); the tokens of sequence s are rows
+ *                query_start[s] .. query_start[s+1]-1, in position order
+ *   query_start  [n_seqs + 1] int32, non-decreasing, query_start[0] >= 0,
+ *                query_start[n_seqs] <= n_tokens
+ *   lens         [n_seqs] int32 context lengths after the chunk (>= the chunk's length)
+ *   out          [n_tokens][n_q][head_dim] double; rows of no sequence are left untouched
+ * Returns 0, or -1 on malformed arguments (as oracle_paged_decode, plus a chunk longer than its
+ * context or a query_start out of order or out of range).
+ */
+int oracle_paged_prefill(int dtype, int n_q, int n_kv, int head_dim, int block_size, int num_blocks,
+                         const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* tables, int max_blocks, const int32_t* lens,
+                         const int32_t* query_start, int n_seqs, int n_tokens,
+                         double scale, double* out, int n_threads) {
+    if (orc_elem_bytes(dtype) == 0 || n_q <= 0 || n_kv <= 0 || n_q % n_kv != 0 || head_dim <= 0 ||
+        block_size <= 0 || n_seqs < 0 || n_tokens < 0)
+        return -1;
+    if (n_seqs > 0 && (query_start[0] < 0 || query_start[n_seqs] > n_tokens)) return -1;
+    const int group = n_q / n_kv;
+    for (int s = 0; s < n_seqs; ++s) {
+        const int n_new = query_start[s + 1] - query_start[s];
+        if (n_new < 0 || lens[s] < n_new || (int64_t)lens[s] > (int64_t)max_blocks * block_size) return -1;
+        int nb = (lens[s] + block_size - 1) / block_size;
+        for (int i = 0; i < nb; ++i) {
+            int32_t x = tables[(size_t)s * max_blocks + i];
+            if (x < 0 || x >= num_blocks) return -1;
+        }
+    }
+    if (n_threads < 1) n_threads = 1;
+    const long n_pairs = (long)n_seqs * n_q;
+    int failed = 0;
+
+#pragma omp parallel for num_threads(n_threads) schedule(dynamic, 1)
+    for (long sh = 0; sh < n_pairs; ++sh) {
+        const int s = (int)(sh / n_q);
+        const int h = (int)(sh % n_q);
+        const int g = h / group;
+        const int c = lens[s];
+        const int n_new = query_start[s + 1] - query_start[s];
+        if (n_new == 0) continue;
+        double* kc = (double*)malloc(sizeof(double) * (size_t)c * head_dim);
+        double* vc = (double*)malloc(sizeof(double) * (size_t)c * head_dim);
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        double* z = (double*)malloc(sizeof(double) * (size_t)c);
+        if (!kc || !vc || !qv || !z) {
+            free(kc); free(vc); free(qv); free(z);
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        /* Gather the sequence's logical rows through its table, once per (sequence, head). */
+        for (int j = 0; j < c; ++j) {
+            int64_t phys = tables[(size_t)s * max_blocks + j / block_size];
+            size_t row = orc_row(phys, g, j % block_size, n_kv, block_size, head_dim);
+            for (int i = 0; i < head_dim; ++i) {
+                kc[(size_t)j * head_dim + i] = orc_load(dtype, k_pool, row + i);
+                vc[(size_t)j * head_dim + i] = orc_load(dtype, v_pool, row + i);
+            }
+        }
+        for (int t = 0; t < n_new; ++t) {
+            const size_t qrow = ((size_t)(query_start[s] + t) * n_q + h) * head_dim;
+            const int pos = c - n_new + t; /* this query's position: it sees keys 0 .. pos */
+            for (int i = 0; i < head_dim; ++i) qv[i] = orc_load(dtype, q, qrow + i);
+            double m = -INFINITY;
+            for (int j = 0; j <= pos; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < head_dim; ++i) acc += qv[i] * kc[(size_t)j * head_dim + i];
+                z[j] = scale * acc;
+                if (z[j] > m) m = z[j];
+            }
+            double zsum = 0.0;
+            for (int j = 0; j <= pos; ++j) {
+                z[j] = exp(z[j] - m);
+                zsum += z[j];
+            }
+            double* o = out + qrow;
+            for (int i = 0; i < head_dim; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j <= pos; ++j) acc += (z[j] / zsum) * vc[(size_t)j * head_dim + i];
+                o[i] = acc;
+            }
         }
         free(kc); free(vc); free(qv); free(z);
     }
