@@ -70,7 +70,8 @@ enum {
     PKV_DEV_BAD_CONTEXT_LEN = 2u, /* context length < 0 or > max_blocks_per_seq*block_size  */
     PKV_DEV_BAD_SLOT = 4u,        /* slot >= num_blocks*block_size                           */
     PKV_DEV_BAD_PAIR = 8u,        /* copy pair id outside [0, num_blocks)                    */
-    PKV_DEV_WAIT_TIMEOUT = 16u    /* a bounded wait on an asynchronous copy gave up          */
+    PKV_DEV_WAIT_TIMEOUT = 16u,   /* a bounded wait on an asynchronous copy gave up          */
+    PKV_DEV_BAD_QUERY_RANGE = 32u /* prefill: query_start / chunk length inconsistent         */
 };
 
 /*
@@ -206,6 +207,42 @@ int pkv_paged_decode_attention_static(const pkv_cache_desc* desc, int32_t layer,
                                       const void* k_pool, const void* v_pool, const int32_t* block_tables,
                                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
                                       float scale, void* out, void* stream);
+
+/*
+ * Paged prefill (or chunked prefill) attention for one layer: a chunk of new query tokens per
+ * sequence attends causally to the sequence's cache through its block table ("PagedAttention e
+ * continuous batching", "01 - Conceito", paragraph 5: a long prompt is processed in slices that
+ * share steps with decoding; "La idea de PagedAttention", step 5: the kernel gathers the rows).
+ * The chunk's K/V rows must already be appended (pkv_kv_append). With c = context_lens[s] and
+ * n_s = query_start[s+1] - query_start[s], chunk token i of sequence s sits at position
+ * p = c - n_s + i and, for query head h and KV head g = h / G,
+ *   out[t][h] = sum_{j <= p} softmax_j(scale * q[t][h] . K_j) V_j,   t = query_start[s] + i,
+ * K_j, V_j being row (block_tables[s][j / 16], g, j mod 16) of layer `layer`: dense causal
+ * attention over the gathered rows. A whole prompt is the chunk n_s == c. fp32 accumulation; out
+ * rounded to desc->dtype.
+ *   q, out        device [n_tokens][n_q_heads][head_dim] of desc->dtype, 16-byte aligned; the
+ *                 chunk tokens of all sequences packed in order (sequence s owns rows
+ *                 query_start[s] .. query_start[s+1]-1, in position order); rows owned by no
+ *                 sequence are left unwritten
+ *   k_pool, v_pool device, whole pools (all layers), 16-byte aligned
+ *   block_tables  device int32 [n_seqs][max_blocks_per_seq]; the first ceil(c/16) entries are read
+ *   context_lens  device int32 [n_seqs]: tokens in the cache after the chunk, n_s <= c <=
+ *                 max_blocks_per_seq*16
+ *   query_start   device int32 [n_seqs + 1], non-decreasing, query_start[0] >= 0,
+ *                 query_start[n_seqs] <= n_tokens
+ *   max_query_len host: the largest n_s (sizes the grid), 0 <= max_query_len <= n_tokens
+ * A sequence whose device-side values break these rules (n_s < 0, n_s > max_query_len, n_s > c,
+ * c too large, query_start outside [0, n_tokens]) is skipped, its rows left unwritten, and sets
+ * PKV_DEV_BAD_QUERY_RANGE. A table entry outside [0, num_blocks) is skipped (its keys count as
+ * masked) and sets PKV_DEV_BAD_BLOCK_ID. Rows past a query's position or past the context are
+ * never used: NaN there cannot reach the output. No workspace; nothing is allocated.
+ * fp16 / bf16 run on the tensor cores; fp32 on the CUDA cores (the precision mode).
+ */
+int pkv_paged_prefill_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
+                                const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                const int32_t* query_start, int32_t n_seqs, int32_t n_tokens,
+                                int32_t max_query_len, float scale, void* out, void* stream);
 
 /*
  * Copy-on-write block copies ("01 - Conceito", paragraph 6): for each pair (src, dst) in

@@ -226,6 +226,49 @@ int pkv_paged_decode_append_attention(const pkv_cache_desc* d, int32_t layer, co
                        n_seqs, scale, out, workspace, workspace_bytes, stream);
 }
 
+int pkv_paged_prefill_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs,
+                                int32_t n_tokens, int32_t max_query_len, float scale, void* out, void* stream) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (layer < 0 || layer >= d->n_layers || n_seqs < 0 || n_tokens < 0 || max_query_len < 0 ||
+        max_query_len > n_tokens)
+        return PKV_ERR_INVALID_ARG;
+    if (n_seqs == 0 || max_query_len == 0) return PKV_OK;
+    if (max_blocks_per_seq <= 0 || max_blocks_per_seq > (1 << 24)) return PKV_ERR_INVALID_ARG;
+    if (n_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (d->dtype != PKV_F32 && (long long)d->num_blocks * d->n_kv_heads * d->block_size >= (1LL << 31))
+        return PKV_ERR_UNSUPPORTED;  // tensor-copy row coordinates are 32-bit
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !query_start || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+
+    pkv::PrefillArgs a;
+    const size_t layer_bytes = layer_elems(d) * elem_bytes(d->dtype);
+    const int group = d->n_q_heads / d->n_kv_heads;
+    const int per_cta = pkv::prefill_tokens_per_cta(d->dtype, d->head_dim, group);
+    a.q = q;
+    a.out = out;
+    a.k_layer = static_cast<const char*>(k_pool) + (size_t)layer * layer_bytes;
+    a.v_layer = static_cast<const char*>(v_pool) + (size_t)layer * layer_bytes;
+    a.tables = block_tables;
+    a.lens = context_lens;
+    a.q_start = query_start;
+    a.n_seqs = n_seqs;
+    a.n_q = d->n_q_heads;
+    a.n_kv = d->n_kv_heads;
+    a.num_blocks = d->num_blocks;
+    a.max_blocks = max_blocks_per_seq;
+    a.n_tokens = n_tokens;
+    a.q_tiles = (max_query_len + per_cta - 1) / per_cta;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t err = pkv::launch_prefill(d->dtype, d->head_dim, group, a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
 int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,
                     void* stream) {
     int rc = pkv_validate_desc(d);

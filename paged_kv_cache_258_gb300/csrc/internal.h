@@ -35,6 +35,32 @@ struct DecodeArgs {
     float scale_log2;       // scale * log2(e): logits are kept in base 2
 };
 
+// Arguments of one paged prefill attention launch (one layer). q / out hold the chunk tokens of
+// all sequences packed in order: sequence s owns rows q_start[s] .. q_start[s+1]-1.
+struct PrefillArgs {
+    const void* q;          // [n_tokens][n_q][D]
+    void* out;              // [n_tokens][n_q][D]
+    const void* k_layer;    // [num_blocks][n_kv][16][D] (the CUDA-core kernel; the MMA kernel uses
+    const void* v_layer;    //  tensor maps of the same layer)
+    const int32_t* tables;  // [n_seqs][max_blocks]
+    const int32_t* lens;    // [n_seqs] context lengths after the chunk
+    const int32_t* q_start; // [n_seqs + 1]
+    unsigned int* status;
+    int n_seqs, n_q, n_kv, num_blocks, max_blocks, n_tokens;
+    int q_tiles;            // CTAs along the chunk: ceil(max query length / tokens per CTA)
+    float scale_log2;       // scale * log2(e)
+};
+
+// Query rows (token x head-in-group) one prefill CTA covers; tokens per CTA = rows / group.
+// Tensor-core kernel: 16 rows per consumer warp, 8 warps (7 at head_dim 256, so that with the
+// producer warp the CTA is 256 threads and a thread may hold 255 registers: the fp32 output
+// accumulator alone is 128 of them). CUDA-core kernel (fp32): 32 rows.
+constexpr int prefill_mma_rows(int head_dim) { return head_dim == 256 ? 112 : 128; }
+constexpr int kPrefillRowsF32 = 32;
+inline int prefill_tokens_per_cta(int dtype, int head_dim, int group) {
+    return (dtype == PKV_F32 ? kPrefillRowsF32 : prefill_mma_rows(head_dim)) / group;
+}
+
 struct AppendArgs {
     const void* k;          // [n_tok][n_kv][D]
     const void* v;
@@ -81,6 +107,10 @@ cudaError_t launch_decode(int dtype, int head_dim, int group, const DecodeArgs& 
 cudaError_t launch_decode_f32(int head_dim, int group, const DecodeArgs& a, cudaStream_t stream, int* n_launches);
 cudaError_t launch_decode_f16(int head_dim, int group, const DecodeArgs& a, cudaStream_t stream, int* n_launches);
 cudaError_t launch_decode_bf16(int head_dim, int group, const DecodeArgs& a, cudaStream_t stream, int* n_launches);
+cudaError_t launch_prefill(int dtype, int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_f32(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 

@@ -1,0 +1,16 @@
+// prefill_f16.cu -- paged prefill attention instantiations for __half storage (tensor cores).
+#include "prefill_mma.cuh"
+
+namespace pkv {
+
+cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream) {
+    const long long rows = (long long)a.num_blocks * a.n_kv * kBlock;
+    if (rows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are 32-bit
+    CUtensorMap tk, tv;
+    cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_F16, &tk);
+    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_F16, &tv);
+    if (err != cudaSuccess) return err;
+    return launch_prefill_mma_dtype<__half>(head_dim, group, a, tk, tv, stream);
+}
+
+}  // namespace pkv
