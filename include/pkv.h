@@ -324,6 +324,19 @@ int pkv_mgr_fork(pkv_mgr* mgr, int64_t parent, int64_t child);
 int pkv_mgr_append_slot(pkv_mgr* mgr, int64_t seq_id, int64_t* slot, int32_t* cow_src, int32_t* cow_dst);
 
 /*
+ * Extend sequence seq_id by n_tokens new tokens at once (one chunk of a chunked prefill, "01 -
+ * Conceito", paragraph 5), all or nothing. slots_out (n_tokens entries, may be NULL when
+ * n_tokens == 0) receives the slots of positions ctx .. ctx+n_tokens-1. The result equals
+ * n_tokens successive pkv_mgr_append_slot calls: only the first token can copy a shared,
+ * partially filled last block (that pair in *cow_src / *cow_dst, else -1; run it through
+ * pkv_copy_blocks before the appends), then fresh blocks are taken in order. If the pool cannot
+ * hold all n_tokens, nothing changes, alloc_failures and append_oom each grow by one and
+ * PKV_ERR_NO_BLOCKS is returned. n_tokens == 0 is a no-op.
+ */
+int pkv_mgr_extend(pkv_mgr* mgr, int64_t seq_id, int32_t n_tokens, int64_t* slots_out, int32_t* cow_src,
+                   int32_t* cow_dst);
+
+/*
  * Append one token to each of seq_ids[0..n) in order. slots_out[n] receives the slots,
  * cow_pairs_out[2*n] the (src, dst) pairs that were emitted, *n_cow their count, *n_done the
  * number of sequences served. Stops at the first failing sequence and returns its status;

@@ -128,6 +128,35 @@ class BlockManagerOracle:
         self.cow_copies += 1
         return "ok", self._slot(b, n), tail, b
 
+    def extend(self, seq_id: int, n_tokens: int):
+        """Extend a sequence by n_tokens at once (one prefill chunk), all or nothing.
+
+        "01 - Conceito" paragraph 5 slices long prompts into chunks. Reading: a chunk succeeds
+        only if the pool holds every block it needs (one more when the first token must copy a
+        shared partial tail); it is then exactly n_tokens appends of step 3. A failing chunk
+        counts one allocation failure and one append OOM and changes nothing.
+        Returns (status, slots, cow_src, cow_dst).
+        """
+        if seq_id not in self.tables or n_tokens < 0:
+            return "invalid", [], -1, -1
+        if n_tokens == 0:
+            return "ok", [], -1, -1
+        table, n = self.tables[seq_id], self.ctx[seq_id]
+        cow = n % self.block_size != 0 and self.ref[table[-1]] > 1
+        need = self._blocks_for(n + n_tokens) - len(table) + (1 if cow else 0)
+        if need > len(self.free):
+            self.alloc_failures += 1
+            self.append_oom += 1
+            return "no_blocks", [], -1, -1
+        slots, src, dst = [], -1, -1
+        for i in range(n_tokens):
+            st, slot, s_, d_ = self.append_slot(seq_id)
+            assert st == "ok"
+            slots.append(slot)
+            if s_ >= 0:
+                src, dst = s_, d_
+        return "ok", slots, src, dst
+
     def free_seq(self, seq_id: int):
         if seq_id not in self.tables:
             return "invalid"

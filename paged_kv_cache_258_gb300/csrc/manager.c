@@ -359,6 +359,71 @@ int pkv_mgr_append_slot(pkv_mgr* m, int64_t seq_id, int64_t* slot, int32_t* cow_
     return PKV_OK;
 }
 
+int pkv_mgr_extend(pkv_mgr* m, int64_t seq_id, int32_t n_tokens, int64_t* slots_out, int32_t* cow_src,
+                   int32_t* cow_dst) {
+    if (!m || n_tokens < 0 || (n_tokens > 0 && !slots_out)) return PKV_ERR_INVALID_ARG;
+    int64_t pos = map_find(m, seq_id);
+    if (pos < 0) return PKV_ERR_INVALID_ARG;
+    if (cow_src) *cow_src = -1;
+    if (cow_dst) *cow_dst = -1;
+    if (n_tokens == 0) return PKV_OK;
+    seq_rec* s = &m->map[pos];
+    const int32_t off = s->ctx % m->block_size;
+    const int cow = off != 0 && m->ref[s->table[s->n_blocks - 1]] > 1;
+    const int64_t end = (int64_t)s->ctx + n_tokens;
+    if (end > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    const int32_t total = blocks_for(m, end);
+    const int32_t fresh = total - s->n_blocks;
+    if ((int64_t)fresh + cow > m->n_free) {
+        m->alloc_failures++;
+        m->append_oom++;
+        return PKV_ERR_NO_BLOCKS;
+    }
+    if (!ensure_table_cap(s, total)) return PKV_ERR_BAD_STATE;
+    /* allocation order of n successive appends: the copy of a shared tail first, then fresh blocks */
+    int32_t cow_block = -1;
+    if (cow) {
+        cow_block = alloc_one(m);
+        if (cow_block < 0) {
+            m->alloc_failures++;
+            m->append_oom++;
+            return PKV_ERR_NO_BLOCKS;
+        }
+    }
+    for (int32_t i = 0; i < fresh; ++i) {
+        int32_t b = alloc_one(m);
+        if (b < 0) { /* injected failure: undo in reverse so the free list is restored exactly */
+            for (int32_t k = i - 1; k >= 0; --k) {
+                m->ref[s->table[s->n_blocks + k]] = 0;
+                ring_push_front(m, s->table[s->n_blocks + k]);
+            }
+            if (cow_block >= 0) {
+                m->ref[cow_block] = 0;
+                ring_push_front(m, cow_block);
+            }
+            m->alloc_failures++;
+            m->append_oom++;
+            return PKV_ERR_NO_BLOCKS;
+        }
+        s->table[s->n_blocks + i] = b;
+    }
+    if (cow_block >= 0) {
+        const int32_t tail = s->table[s->n_blocks - 1];
+        m->ref[tail]--;
+        s->table[s->n_blocks - 1] = cow_block;
+        m->cow_copies++;
+        if (cow_src) *cow_src = tail;
+        if (cow_dst) *cow_dst = cow_block;
+    }
+    s->n_blocks = total;
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        const int64_t p = (int64_t)s->ctx + i;
+        slots_out[i] = (int64_t)s->table[p / m->block_size] * m->block_size + p % m->block_size;
+    }
+    s->ctx = (int32_t)end;
+    return PKV_OK;
+}
+
 int pkv_mgr_append_batch(pkv_mgr* m, const int64_t* seq_ids, int32_t n, int64_t* slots_out,
                          int32_t* cow_pairs_out, int32_t* n_cow, int32_t* n_done) {
     if (!m || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out))) return PKV_ERR_INVALID_ARG;

@@ -87,6 +87,7 @@ def lib():
         "pkv_mgr_fork": (ctypes.c_int, [vp, c_i64, c_i64]),
         "pkv_mgr_append_slot": (ctypes.c_int, [vp, c_i64, i64p, i32p, i32p]),
         "pkv_mgr_append_batch": (ctypes.c_int, [vp, i64p, c_i32, i64p, i32p, i32p, i32p]),
+        "pkv_mgr_extend": (ctypes.c_int, [vp, c_i64, c_i32, i64p, i32p, i32p]),
         "pkv_mgr_free_seq": (ctypes.c_int, [vp, c_i64]),
         "pkv_mgr_block_table": (ctypes.c_int, [vp, c_i64, i32p, c_i32, i32p, i32p]),
         "pkv_mgr_pack_tables": (ctypes.c_int, [vp, i64p, c_i32, c_i32, i32p, i32p]),
@@ -352,6 +353,14 @@ class BlockManager:
 
     def fork(self, parent: int, child: int) -> int:
         return lib().pkv_mgr_fork(self._h, int(parent), int(child))
+
+    def extend(self, seq_id: int, n_tokens: int, slots_out=None):
+        """Slots of n_tokens new positions at once (all or nothing); returns (rc, slots, src, dst)."""
+        n = int(n_tokens)
+        slots = slots_out if slots_out is not None else np.zeros(max(n, 1), dtype=np.int64)
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        rc = lib().pkv_mgr_extend(self._h, int(seq_id), n, _i64p(slots), ctypes.byref(src), ctypes.byref(dst))
+        return rc, (slots[:n] if rc == PKV_OK else slots[:0]), int(src.value), int(dst.value)
 
     def append_slot(self, seq_id: int):
         slot, src, dst = ctypes.c_int64(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)

@@ -45,6 +45,12 @@ def apply_both(c, o, op):
         assert status(rc) == st
         if st == "ok":
             assert (slot, src, dst) == (slot_o, src_o, dst_o)
+    elif kind == "extend":
+        rc, slots, src, dst = c.extend(op[1], op[2])
+        st, want, src_o, dst_o = o.extend(op[1], op[2])
+        assert status(rc) == st
+        if st == "ok":
+            assert (slots.tolist(), src, dst) == (want, src_o, dst_o)
     elif kind == "free":
         assert status(c.free_seq(op[1])) == o.free_seq(op[1])
     else:
@@ -90,8 +96,10 @@ def test_random_logs_bitexact(seed):
         elif r < 0.22:
             op = ("fork", rng.choice(live), next_id)
             next_id += 1
-        elif r < 0.85:
+        elif r < 0.78:
             op = ("append", rng.choice(live + [10 ** 9]))
+        elif r < 0.85:
+            op = ("extend", rng.choice(live + [10 ** 9]), rng.choice([0, 1, 5, 16, 37, 200]))
         else:
             op = ("free", rng.choice(live + [-5]))
         apply_both(c, o, op)
@@ -117,6 +125,47 @@ def test_append_batch_matches_single_appends():
                 want_pairs.append([src, dst])
         assert pairs.tolist() == want_pairs
         compare(c, o)
+
+
+def test_extend_equals_successive_appends_and_is_all_or_nothing():
+    order = W.free_order(40, 4)
+    c, o = pkv.BlockManager(40, free_order=order), BlockManagerOracle(40, free_order=order)
+    apply_both(c, o, ("add", 0, 20))
+    apply_both(c, o, ("fork", 0, 1))
+    apply_both(c, o, ("fork", 0, 2))
+    # chunk into a shared partial tail: one copy, then fresh blocks, slots in position order
+    rc, slots, src, dst = c.extend(1, 50)
+    assert rc == pkv.PKV_OK and src == o.tables[0][-1] and dst >= 0
+    st, want, src_o, dst_o = o.extend(1, 50)
+    assert (st, slots.tolist(), src, dst) == ("ok", want, src_o, dst_o)
+    compare(c, o)
+    # a chunk the pool cannot hold changes nothing (counts one failure and one append OOM)
+    before = (c.free_list(), c.refcounts(), c.block_table(2))
+    rc, slots, src, dst = c.extend(2, 16 * 40)
+    assert rc == pkv.PKV_ERR_NO_BLOCKS and len(slots) == 0
+    assert o.extend(2, 16 * 40)[0] == "no_blocks"
+    assert (c.free_list(), c.refcounts(), c.block_table(2)) == before
+    compare(c, o)
+    # a cloned manager replaying the chunk as single appends ends in the same state
+    c2 = c.clone()
+    rc, slots, _, _ = c.extend(2, 33)
+    singles = [c2.append_slot(2) for _ in range(33)]
+    assert [s_[1] for s_ in singles] == slots.tolist()
+    assert c2.free_list() == c.free_list() and c2.stats() == c.stats()
+
+
+def test_injected_failure_in_extend_rolls_back():
+    c = pkv.BlockManager(12)
+    assert c.add_seq(0, 20)[0] == pkv.PKV_OK
+    assert c.fork(0, 1) == pkv.PKV_OK
+    before = (c.free_list(), c.refcounts(), c.block_table(0), c.block_table(1))
+    for after in range(4):                             # the copy, then each fresh block
+        c.inject_alloc_failure(after)
+        rc, _, _, _ = c.extend(1, 60)
+        assert rc == pkv.PKV_ERR_NO_BLOCKS
+        assert (c.free_list(), c.refcounts(), c.block_table(0), c.block_table(1)) == before
+    rc, slots, src, dst = c.extend(1, 60)
+    assert rc == pkv.PKV_OK and src >= 0 and len(slots) == 60
 
 
 def test_append_batch_stops_at_first_failure():
