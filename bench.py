@@ -1,6 +1,6 @@
 """Benchmark: paged decode attention on one GB300 (KV GB/s, decode tokens/s, % of HBM roofline).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gpt|ragged|longdoc|prefix]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gpt|ragged|longdoc|prefix|prefill30k]
                     [--impl pkv|reference]
 
 A step is one decode step of the whole hot path over one batch: the host block manager
@@ -10,6 +10,9 @@ the attention read per step (sum of context lengths x 2 x n_kv x head_dim x byte
 divided by the step time, with the step's inputs already in HBM; ``e2e`` is the same metric
 with the per-step inputs (q, new K/V rows for every layer) copied from pinned host memory and
 the outputs copied back inside the timed region.
+
+--config prefill30k prints the chunked-prefill line instead: one 30,000-token prompt of the
+long-document model prefilled in chunks of 2,048 tokens, ``value`` = causal attention TFLOP/s.
 
 Every input is synthetic and seeded (see paged_kv_cache_258_gb300/workloads.py). Multi-GPU
 (torchrun) runs one independent replica per rank (weak scaling: sequences shard across ranks
@@ -379,6 +382,195 @@ def run_gpu(args) -> dict | None:
     return line
 
 
+# ---------------------------------------------------------------------------------------------
+# chunked prefill of one long prompt ("01 - Conceito", paragraph 5: a 30,000-token prompt is
+# processed in slices); the model is the long-document one (16 layers, 16 query / 4 KV heads x 256,
+# bf16). The chunk size is not on the pages: 2,048 tokens per chunk.
+
+PREFILL_METRIC = "paged prefill attention TFLOP/s (causal) at 1 GB300; % of tensor roofline"
+PREFILL = dict(n_layers=16, n_q=16, n_kv=4, d=256, dtype="bf16", prompt=30000, chunk=2048)
+
+
+def prefill_chunks(prompt: int, chunk: int):
+    return [(c0, min(chunk, prompt - c0)) for c0 in range(0, prompt, chunk)]
+
+
+def run_prefill_gpu(args) -> dict | None:
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+    from paged_kv_cache_258_gb300.engine import PagedKVCache, PrefillStep
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    P = dict(PREFILL)
+    if args.layers:
+        P["n_layers"] = args.layers
+    L, n_q, n_kv, d, prompt, chunk = P["n_layers"], P["n_q"], P["n_kv"], P["d"], P["prompt"], P["chunk"]
+    seed = W.BASE_SEED + 5 + rank
+    nb_seq = -(-prompt // W.BLOCK)
+    num_blocks = int(nb_seq * 1.125) + 1
+    desc = pkv.make_desc(P["dtype"], L, num_blocks, n_q, n_kv, d)
+    order = W.free_order(num_blocks, seed) if args.placement == "shuffled" else None
+    cache = PagedKVCache(desc, free_order=order, device=device)
+    ps = PrefillStep(cache, max_tokens=chunk, max_seqs=1, max_blocks=nb_seq)
+    stream = ps.stream
+    dt = pkv.torch_dtype(P["dtype"])
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = torch.randn((L, prompt, n_q, d), device=device, generator=g).to(dt)
+    k_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
+    v_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
+    out = torch.empty_like(q)
+    scale = 1.0 / float(np.sqrt(d))
+    chunks = prefill_chunks(prompt, chunk)
+    seq = 1
+
+    def one_step(on_attn=None, bufs=None):
+        nonlocal seq
+        flops = 0.0
+        for i, (c0, n) in enumerate(chunks):
+            if bufs is not None:
+                bufs(c0, n)
+            st = ps.step([(seq, n, i == 0)], q[:, c0:c0 + n], k_new[:, c0:c0 + n], v_new[:, c0:c0 + n],
+                         out[:, c0:c0 + n], scale, on_attn)
+            flops += PrefillStep.attention_flops(st, n_q, d) * L
+        cache.free(seq)       # host only: the next step admits the prompt again
+        seq += 1
+        return flops
+
+    for _ in range(args.warmup):
+        one_step()
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError("device status flags during warm-up")
+
+    n_launch = args.steps * len(chunks) * L
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_launch)]
+    cur = {"i": 0}
+
+    def on_attn(layer, when):
+        e = ev[cur["i"]]
+        if when == "start":
+            e[0].record(stream)
+        else:
+            e[1].record(stream)
+            cur["i"] += 1
+
+    sampler = ClockSampler(gpu_uuid(local))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.pkv_launch_count()
+    flops = 0.0
+    t0.record(stream)
+    for _ in range(args.steps):
+        flops += one_step(on_attn)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = pkv.pkv_launch_count() - launches0
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError("device status flags set during the timed region")
+    ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
+    total_flops = reduce_over_ranks(flops, "sum", device)
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev)
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+
+    # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory, outputs back
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k_new, v_new))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def bufs(c0, n):
+        with torch.cuda.stream(stream):
+            q[:, c0:c0 + n].copy_(hq[:, c0:c0 + n], non_blocking=True)
+            k_new[:, c0:c0 + n].copy_(hk[:, c0:c0 + n], non_blocking=True)
+            v_new[:, c0:c0 + n].copy_(hv[:, c0:c0 + n], non_blocking=True)
+
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_flops = 0.0
+    for _ in range(args.steps):
+        e2e_flops += one_step(bufs=bufs)
+        with torch.cuda.stream(stream):
+            hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", device)
+    e2e_flops = reduce_over_ranks(e2e_flops, "sum", device)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    peak_src = "measured bf16_tflops_sustained (cuBLAS bf16 GEMM, seconds-long loop)" \
+        if "bf16_tflops_sustained" in peaks else "fallback 1.7 PFLOP/s sustained"
+    value = total_flops / (ms * 1e-3) / 1e12
+    elem = 2
+    h2d = (q.numel() + k_new.numel() + v_new.numel()) * elem
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q and K/V rows)",
+        "config": {"workload": f"prefill30k: one {prompt}-token prompt in {len(chunks)} chunks of {chunk} tokens, "
+                               f"{L} layers x {n_q} q / {n_kv} kv heads x head_dim {d} bf16, block 16",
+                   "step": "per chunk: manager admit/extend, one metadata upload, per layer kv_append + "
+                           "paged prefill attention",
+                   "l2": "no flush: each step streams 5.9 GB of new rows and 1 GiB of cache per layer set",
+                   "parallelism": f"replicas x{ws} (one prompt per rank, no collective)",
+                   "placement": args.placement},
+        "prompt_tokens_per_s": round(prompt * args.steps * ws / (ms * 1e-3), 1),
+        "roofline": {"kernel": "paged_prefill_mma_kernel (mma.sync m16n8k16, TMA producer warp)",
+                     "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "launch_ms_mean": round(attn_ms / n_launch, 4),
+                     "algorithmic_flops_per_launch": int(flops / n_launch)},
+        "e2e": {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * elem),
+                "ms_per_step": round(e2e_ms / args.steps, 3)},
+        "gpu_launches": int(launches),
+        "host_manager_us_per_step": round(ps.manager_s / max(1, (args.warmup + 2 * args.steps)) * 1e6, 1),
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_sample(cache, budget_s=args.cpu_budget, P=P, seed=seed)
+    return line
+
+
+def prefill_cpu_sample(cache=None, budget_s: float = 12.0, P=None, seed: int = 0) -> dict:
+    """The fp64 oracle's prefill, as it stands, on this host's cores: blocks of 64 queries of the
+    prompt's last chunk (the costliest positions) on one layer, until the budget is spent."""
+    import oracle
+    P = P or PREFILL
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(seed + 17)
+    prompt, n_q, n_kv, d, dtype = P["prompt"], P["n_q"], P["n_kv"], P["d"], P["dtype"]
+    nb = -(-prompt // W.BLOCK)
+    tables = W.shuffled_tables(np.array([prompt], dtype=np.int32), nb, seed)
+    kp = W.normal_values(rng, (nb, n_kv, W.BLOCK, d), dtype)
+    vp = W.normal_values(rng, (nb, n_kv, W.BLOCK, d), dtype)
+    flops, el, done = 0.0, 0.0, 0
+    last0 = prompt - (prompt % P["chunk"] or P["chunk"])
+    while el < budget_s and last0 + done + 64 <= prompt:
+        c = last0 + done + 64                       # the cache holds positions 0 .. c-1
+        q = W.normal_values(rng, (64, n_q, d), dtype)
+        t0 = time.perf_counter()
+        oracle.paged_prefill(dtype, q, kp, vp, tables, np.array([c], np.int32), np.array([0, 64], np.int32),
+                             1.0 / np.sqrt(d), n_threads=threads)
+        el += time.perf_counter() - t0
+        flops += 4.0 * d * n_q * (64 * (c - 64) + 64 * 65 / 2)
+        done += 64
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} queries of the last chunk (positions {last0}..{last0 + done - 1}), 1 layer, "
+                      f"{n_q} heads (fp64 C oracle, OpenMP over (sequence, head)); {el:.1f} s"}
+
+
 def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
     import torch
     q, k_new, v_new, out = bufs
@@ -526,12 +718,39 @@ def run_reference(args) -> dict | None:
     }
 
 
+def run_prefill_reference(args) -> dict | None:
+    """Reference arm of the prefill line: the fp64 oracle, as it stands, on a bounded sample."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    per_step = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        prefill_cpu_sample(budget_s=per_step / 4, seed=W.BASE_SEED + 5)
+    t0 = time.perf_counter()
+    samples = [prefill_cpu_sample(budget_s=per_step, seed=W.BASE_SEED + 5) for _ in range(args.steps)]
+    el = time.perf_counter() - t0
+    value = statistics.median(s_["value"] for s_ in samples)
+    cb = dict(samples[0])
+    cb["value"] = value
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "prefill30k (bounded sample: queries of the last chunk, one layer)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="gpt", choices=["gpt", "ragged", "longdoc", "prefix"])
+    ap.add_argument("--config", default="gpt", choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
@@ -542,7 +761,9 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
-        line = run_reference(args)
+        line = run_prefill_reference(args) if args.config == "prefill30k" else run_reference(args)
+    elif args.config == "prefill30k":
+        line = run_prefill_gpu(args)
     else:
         line = run_gpu(args)
     if line is not None:

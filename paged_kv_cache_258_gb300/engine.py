@@ -1,7 +1,7 @@
-"""A paged KV cache on one GPU and its decode step, on top of the C ABI.
+"""A paged KV cache on one GPU, its decode step and its chunked-prefill step, on top of the C ABI.
 
 ``PagedKVCache`` owns the all-layer K/V pools (torch device memory) and the host C block
-manager. ``DecodeBatch`` runs decode steps for a fixed list of sequences in the order the
+manager. ``PrefillStep`` (at the end of this module) runs chunked prefill. ``DecodeBatch`` runs decode steps for a fixed list of sequences in the order the
 method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAttention", steps
 3 and 5; "PagedAttention e continuous batching", "01 - Conceito", paragraph 6):
 
@@ -192,3 +192,137 @@ class DecodeBatch:
         """Algorithmic KV bytes the last step's attention read: sum(ctx) * 2 * n_kv * d * e * L."""
         return int(self.last_lens.astype(np.int64).sum()) * self.cache.kv_bytes_per_token_layer() * \
             self.cache.desc.n_layers
+
+
+class PrefillStep:
+    """Chunked-prefill steps: each listed sequence gains a chunk of new tokens.
+
+    "PagedAttention e continuous batching", "01 - Conceito", paragraph 5: long prompts are
+    processed in slices so that they share steps with everyone else's decoding. One step:
+
+      1. host:   a sequence's first chunk admits it (pkv_mgr_add_seq: blocks for the chunk
+                 only); a later chunk extends it (pkv_mgr_extend, all or nothing, copying a
+                 shared partial tail if there is one); the tables are packed;
+      2. H2D:    slots, tables, lengths, query offsets and copy pairs in one copy (pinned,
+                 double-buffered as in DecodeBatch);
+      3. device: copy-on-write block copies, then per layer the KV append of the chunk rows and
+                 the paged prefill attention (the chunk attends causally to everything cached).
+
+    Capacity is fixed at construction: at most max_tokens chunk tokens and max_seqs sequences
+    per step, tables at most max_blocks wide.
+    """
+
+    def __init__(self, cache: PagedKVCache, max_tokens: int, max_seqs: int, max_blocks: int, stream=None):
+        import torch
+        self.cache = cache
+        self.max_tokens, self.max_seqs, self.max_blocks = int(max_tokens), int(max_seqs), int(max_blocks)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
+        T, S, mb = self.max_tokens, self.max_seqs, self.max_blocks
+        # [slots int64 (2T words) | tables S*mb | lens S | query_start S+1 | pairs 2S]
+        self._o_tab = 2 * T
+        self._o_len = self._o_tab + S * mb
+        self._o_qs = self._o_len + S
+        self._o_pair = self._o_qs + S + 1
+        self._words = self._o_pair + 2 * S
+        self.d_meta = torch.empty(self._words, dtype=torch.int32, device=cache.device)
+        self._stage = []
+        for _ in range(2):
+            h = torch.empty(self._words, dtype=torch.int32).pin_memory()
+            self._stage.append(dict(meta=h, np=h.numpy(), done=torch.cuda.Event(), used=False))
+        self._turn = 0
+        self.manager_s = 0.0
+
+    def _dev_views(self, n_seqs: int, n_tok: int):
+        import torch
+        m = self.d_meta
+        S, mb = self.max_seqs, self.max_blocks
+        return (m[: 2 * n_tok].view(torch.int64),
+                m[self._o_tab: self._o_tab + S * mb].view(S, mb)[:n_seqs],
+                m[self._o_len: self._o_len + n_seqs],
+                m[self._o_qs: self._o_qs + n_seqs + 1],
+                m[self._o_pair:].view(-1, 2))
+
+    def plan(self, chunks) -> dict:
+        """chunks: list of (seq_id, n_tokens, first) -- first=True admits the sequence."""
+        n_seqs = len(chunks)
+        n_tok = int(sum(c[1] for c in chunks))
+        if n_seqs > self.max_seqs or n_tok > self.max_tokens or n_seqs == 0:
+            raise ValueError("chunk set exceeds the step's capacity")
+        st = self._stage[self._turn]
+        self._turn ^= 1
+        if st["used"]:
+            st["done"].synchronize()
+        t0 = time.perf_counter()
+        meta = st["np"]
+        slots = meta[: 2 * self.max_tokens].view(np.int64)
+        qs = meta[self._o_qs: self._o_qs + n_seqs + 1]
+        pairs = meta[self._o_pair:].reshape(-1, 2)
+        mgr = self.cache.mgr
+        npairs, pos, max_q = 0, 0, 0
+        qs[0] = 0
+        for i, (sid, n, first) in enumerate(chunks):
+            n = int(n)
+            if first:
+                rc, got = mgr.add_seq(sid, n)
+                if rc == pkv.PKV_OK:
+                    slots[pos: pos + n] = got
+                src = -1
+            else:
+                rc, _, src, dst = mgr.extend(sid, n, slots_out=slots[pos:])
+            if rc != pkv.PKV_OK:
+                raise pkv.PkvError(rc, f"prefill chunk of sequence {sid} ({n} tokens)")
+            if src >= 0:
+                pairs[npairs] = (src, dst)
+                npairs += 1
+            pos += n
+            qs[i + 1] = pos
+            max_q = max(max_q, n)
+        ids = np.ascontiguousarray([c[0] for c in chunks], dtype=np.int64)
+        tables = meta[self._o_tab: self._o_tab + n_seqs * self.max_blocks]
+        lens = meta[self._o_len: self._o_len + n_seqs]
+        rc, _, _ = mgr.pack_tables(ids, self.max_blocks, tables, lens)
+        if rc != pkv.PKV_OK:
+            raise pkv.PkvError(rc, "pack_tables (is max_blocks wide enough?)")
+        self.manager_s += time.perf_counter() - t0
+        st.update(n_seqs=n_seqs, n_tok=n_tok, npairs=npairs, max_q=max_q, lens=lens.copy(), qs=qs.copy())
+        return st
+
+    def upload(self, st: dict) -> None:
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.d_meta.copy_(st["meta"], non_blocking=True)
+            st["done"].record(self.stream)
+        st["used"] = True
+
+    def run_device(self, st: dict, q, k_new, v_new, out, scale: float, on_attn=None) -> None:
+        """q/out [L, T, n_q, d], k_new/v_new [L, T, n_kv, d] (T = the step's chunk tokens)."""
+        c = self.cache
+        d = c.desc
+        slots, tables, lens, qs, pairs = self._dev_views(st["n_seqs"], st["n_tok"])
+        if st["npairs"]:
+            pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, pairs[: st["npairs"]], stream=self.stream)
+        for layer in range(d.n_layers):
+            pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], slots, c.k_pool, c.v_pool, stream=self.stream)
+            if on_attn is not None:
+                on_attn(layer, "start")
+            pkv.pkv_paged_prefill_attention(d, layer, q[layer], c.k_pool, c.v_pool, tables, lens, qs, st["max_q"],
+                                            scale, out[layer], stream=self.stream)
+            if on_attn is not None:
+                on_attn(layer, "end")
+
+    def step(self, chunks, q, k_new, v_new, out, scale: float, on_attn=None) -> dict:
+        st = self.plan(chunks)
+        self.upload(st)
+        self.run_device(st, q, k_new, v_new, out, scale, on_attn)
+        return st
+
+    @staticmethod
+    def attention_flops(st: dict, n_q: int, head_dim: int) -> float:
+        """Causal attention flops of one layer: 4 * d * n_q * sum over chunk tokens of (position + 1)."""
+        total = 0.0
+        for s in range(st["n_seqs"]):
+            n = int(st["qs"][s + 1] - st["qs"][s])
+            c = int(st["lens"][s])
+            # positions c-n .. c-1 see c-n+1 .. c keys
+            total += n * (c - n) + n * (n + 1) / 2
+        return 4.0 * head_dim * n_q * total

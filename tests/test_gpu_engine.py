@@ -98,3 +98,73 @@ def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d, fused):
     assert cow_seen >= n_members                      # every member copied its shared tail once
     assert pkv.pkv_get_device_status() == 0
     assert cache.mgr.stats() == mo.stats()
+
+
+@pytest.mark.parametrize("dtype,n_q,n_kv,d", [("bf16", 8, 2, 128), ("f16", 4, 4, 64), ("f32", 4, 2, 64)])
+def test_chunked_prefill_steps_match_oracle(dtype, n_q, n_kv, d):
+    """Chunked prefill through the engine: admissions, extends and copy-on-write of a shared tail,
+    C manager vs oracle manager bit for bit, attention vs the oracle on its own host pools."""
+    from paged_kv_cache_258_gb300.engine import PrefillStep
+    rng = np.random.default_rng(91)
+    L, nb = 2, 220
+    order = W.free_order(nb, 8)
+    desc = pkv.make_desc(dtype, L, nb, n_q, n_kv, d)
+    cache = PagedKVCache(desc, free_order=order)
+    mo = BlockManagerOracle(nb, free_order=order)
+    hk = np.zeros((L, nb, n_kv, 16, d), NP_STORAGE[dtype])
+    hv = np.zeros_like(hk)
+    ps = PrefillStep(cache, max_tokens=300, max_seqs=4, max_blocks=40)
+    scale = 1.0 / np.sqrt(d)
+    plan = [
+        [(100, 37, True), (1, 128, True), (2, 70, True)],
+        "fork",
+        [(1, 128, False), (10, 50, False), (11, 20, False)],
+        [(1, 44, False), (10, 30, False), (2, 1, False), (3, 200, True)],
+    ]
+    cow_seen = 0
+    for chunks in plan:
+        if chunks == "fork":
+            for child in (10, 11):
+                cache.fork(100, child)
+                assert mo.fork(100, child) == "ok"
+            continue
+        T = sum(c[1] for c in chunks)
+        q = W.normal_values(rng, (L, T, n_q, d), dtype)
+        kn = W.normal_values(rng, (L, T, n_kv, d), dtype)
+        vn = W.normal_values(rng, (L, T, n_kv, d), dtype)
+        out = torch.full((L, T, n_q, d), float("nan"), dtype=pkv.torch_dtype(dtype), device="cuda")
+        st = ps.step(chunks, to_torch(q, dtype), to_torch(kn, dtype), to_torch(vn, dtype), out, scale)
+        got_slots = st["np"][: 2 * ps.max_tokens].view(np.int64)[:T].tolist()
+        slots_o, pairs_o = [], []
+        for sid, n, first in chunks:
+            if first:
+                s_, sl = mo.add_seq(sid, n)
+            else:
+                s_, sl, src, dst = mo.extend(sid, n)
+                if src >= 0:
+                    pairs_o.append((src, dst))
+            assert s_ == "ok"
+            slots_o += list(sl)
+        assert got_slots == slots_o
+        assert st["npairs"] == len(pairs_o)
+        cow_seen += len(pairs_o)
+        if pairs_o:
+            oracle.copy_blocks(hk, hv, np.array(pairs_o, dtype=np.int32))
+        ids = [c[0] for c in chunks]
+        tables = np.full((len(ids), ps.max_blocks), -1, dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        for i, sid in enumerate(ids):
+            t_o, ctx_o = mo.block_table(sid)
+            tables[i, : len(t_o)] = t_o
+            lens[i] = ctx_o
+        assert np.array_equal(st["lens"], lens)
+        qs = np.concatenate([[0], np.cumsum([c[1] for c in chunks])]).astype(np.int32)
+        got = as_f64(out)
+        for layer in range(L):
+            oracle.kv_append(kn[layer], vn[layer], np.array(slots_o), hk[layer], hv[layer])
+            want = oracle.paged_prefill(dtype, q[layer], hk[layer], hv[layer], tables, lens, qs, scale)
+            err = np.max(np.abs(got[layer] - want))
+            assert err <= TOL[dtype], f"layer {layer}: {err:.3e}"
+    assert cow_seen == 2                       # both forks copied the root's partial tail once
+    assert pkv.pkv_get_device_status() == 0
+    assert cache.mgr.stats() == mo.stats()
