@@ -326,3 +326,114 @@ class PrefillStep:
             # positions c-n .. c-1 see c-n+1 .. c keys
             total += n * (c - n) + n * (n + 1) / 2
         return 4.0 * head_dim * n_q * total
+
+
+class StepExecutor:
+    """Runs one continuous-batching iteration planned by scheduler.Scheduler on the device.
+
+    The plan arrives complete (slots, tables, lengths, query offsets, copy pairs: every manager
+    call has been made on the host). One packed metadata image goes up in one copy; then the
+    copy-on-write block copies, and per layer the chunk rows' append + paged prefill attention for
+    the prefilling sequences and the fused append + paged decode attention for the decoding ones.
+    Capacities (decoders, chunk tokens, chunks, copy pairs per iteration; table width) are fixed
+    at construction.
+    """
+
+    def __init__(self, cache: PagedKVCache, max_decode: int, max_tokens: int, max_chunks: int, max_blocks: int,
+                 max_pairs: int | None = None, stream=None):
+        import torch
+        self.cache = cache
+        self.D, self.T, self.S, self.mb = int(max_decode), int(max_tokens), int(max_chunks), int(max_blocks)
+        self.P = int(max_pairs) if max_pairs is not None else self.D + self.S
+        self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
+        D, T, S, mb, P = self.D, self.T, self.S, self.mb, self.P
+        o = {}
+        off = 0
+        for name, words in (("dec_slots", 2 * D), ("pre_slots", 2 * T), ("dec_tables", D * mb), ("dec_lens", D),
+                            ("pre_tables", S * mb), ("pre_lens", S), ("pre_qs", S + 1), ("pairs", 2 * P)):
+            o[name] = (off, words)
+            off += words + (words & 1)          # keep int64 fields 8-byte aligned
+        self._off, self._words = o, off
+        self.d_meta = torch.empty(off, dtype=torch.int32, device=cache.device)
+        self._stage = []
+        for _ in range(2):
+            h = torch.empty(off, dtype=torch.int32).pin_memory()
+            self._stage.append(dict(meta=h, np=h.numpy(), done=torch.cuda.Event(), used=False))
+        self._turn = 0
+        self.workspace = pkv.alloc_workspace(cache.desc, max(D, 1), mb, device=cache.device)
+
+    def _host(self, np_meta, name, dtype=np.int32):
+        off, words = self._off[name]
+        v = np_meta[off: off + words]
+        return v.view(np.int64) if dtype == np.int64 else v
+
+    def _dev(self, name, n=None, shape=None, i64=False):
+        import torch
+        off, words = self._off[name]
+        v = self.d_meta[off: off + words]
+        if i64:
+            v = v.view(torch.int64)
+        if n is not None:
+            v = v[:n]
+        if shape is not None:
+            v = v.view(*shape)
+        return v
+
+    def upload(self, plan) -> dict:
+        import torch
+        n_dec, n_pre, n_tok, n_pairs = plan.n_dec, len(plan.pre_chunks), plan.n_pre_tokens, len(plan.pairs)
+        if n_dec > self.D or n_tok > self.T or n_pre > self.S or n_pairs > self.P:
+            raise ValueError("iteration exceeds the executor's capacity")
+        st = self._stage[self._turn]
+        self._turn ^= 1
+        if st["used"]:
+            st["done"].synchronize()
+        m = st["np"]
+        self._host(m, "dec_slots", np.int64)[:n_dec] = plan.dec_slots
+        self._host(m, "pre_slots", np.int64)[:n_tok] = plan.pre_slots
+        self._host(m, "dec_tables")[: n_dec * self.mb] = plan.dec_tables.reshape(-1)
+        self._host(m, "dec_lens")[:n_dec] = plan.dec_lens
+        self._host(m, "pre_tables")[: n_pre * self.mb] = plan.pre_tables.reshape(-1)
+        self._host(m, "pre_lens")[:n_pre] = plan.pre_lens
+        self._host(m, "pre_qs")[: n_pre + 1] = plan.pre_qs
+        self._host(m, "pairs")[: 2 * n_pairs] = plan.pairs.reshape(-1)
+        with torch.cuda.stream(self.stream):
+            self.d_meta.copy_(st["meta"], non_blocking=True)
+            st["done"].record(self.stream)
+        st["used"] = True
+        return dict(n_dec=n_dec, n_pre=n_pre, n_tok=n_tok, n_pairs=n_pairs,
+                    max_q=max([n for _, n in plan.pre_chunks], default=0))
+
+    def run(self, plan, dec_io, pre_io, scale: float, on_kernel=None) -> dict:
+        """dec_io = (q [L, n_dec, n_q, d], k, v [L, n_dec, n_kv, d], out like q); pre_io the same with
+        the iteration's chunk tokens in place of n_dec. Views of larger resident buffers are fine."""
+        c = self.cache
+        d = c.desc
+        u = self.upload(plan)
+        if u["n_pairs"]:
+            pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self._dev("pairs", 2 * u["n_pairs"], (-1, 2)),
+                                stream=self.stream)
+        for layer in range(d.n_layers):
+            if u["n_pre"]:
+                q, k, v, out = (t[layer] for t in pre_io)
+                pkv.pkv_kv_append(d, layer, k, v, self._dev("pre_slots", u["n_tok"], i64=True), c.k_pool, c.v_pool,
+                                  stream=self.stream)
+                if on_kernel is not None:
+                    on_kernel("prefill", layer, "start")
+                pkv.pkv_paged_prefill_attention(
+                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * self.mb, (-1, self.mb)),
+                    self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
+                    stream=self.stream)
+                if on_kernel is not None:
+                    on_kernel("prefill", layer, "end")
+            if u["n_dec"]:
+                q, k, v, out = (t[layer] for t in dec_io)
+                if on_kernel is not None:
+                    on_kernel("decode", layer, "start")
+                pkv.pkv_paged_decode_append_attention(
+                    d, layer, q, k, v, c.k_pool, c.v_pool,
+                    self._dev("dec_tables", u["n_dec"] * self.mb, (-1, self.mb)), self._dev("dec_lens", u["n_dec"]),
+                    scale, out, self.workspace, stream=self.stream)
+                if on_kernel is not None:
+                    on_kernel("decode", layer, "end")
+        return u
