@@ -718,6 +718,178 @@ def run_reference(args) -> dict | None:
     }
 
 
+# ---------------------------------------------------------------------------------------------
+# continuous batching ("01 - Conceito", paragraphs 5-8): Poisson arrivals of two request classes on
+# the GPT-style model of "Configurando as Constantes"; the loop synchronises every iteration to
+# timestamp its tokens, as a serving loop does. Attention and cache management only: no model
+# weights run, q and the new K/V rows are synthetic.
+
+SERVE_METRIC = "continuous batching on the paged KV cache: generated tokens/s at 1 GB300 (attention + cache only)"
+SERVE = dict(n_layers=32, n_q=32, n_kv=32, d=128, dtype="f16", num_blocks=16384, n_requests=192, rate=48.0,
+             max_batch_tokens=2048, chunk=512, max_running=160, max_blocks=1024, seed=W.BASE_SEED + 6)
+
+
+def serve_trace(P):
+    from paged_kv_cache_258_gb300.scheduler import synthetic_trace
+    reqs = synthetic_trace(P["n_requests"], seed=P["seed"], rate_per_s=P["rate"],
+                           classes=[("chat", 0.85, 1), ("doc", 0.15, 0)])
+    rng = np.random.default_rng(P["seed"] + 1)
+    for r in reqs:
+        if r.klass == "doc":                      # long documents: 2k..8k-token prompts
+            r.prompt = int(rng.integers(2048, 8193))
+    return reqs
+
+
+def run_serve_gpu(args) -> dict | None:
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+    from paged_kv_cache_258_gb300.engine import PagedKVCache, StepExecutor
+    from paged_kv_cache_258_gb300.scheduler import Scheduler, serve
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    P = dict(SERVE)
+    if args.layers:
+        P["n_layers"] = args.layers
+    L, n_q, n_kv, d = P["n_layers"], P["n_q"], P["n_kv"], P["d"]
+    desc = pkv.make_desc(P["dtype"], L, P["num_blocks"], n_q, n_kv, d)
+    order = W.free_order(P["num_blocks"], P["seed"] + rank)
+    cache = PagedKVCache(desc, free_order=order, device=device)
+    D, T = P["max_running"], P["max_batch_tokens"]
+    ex = StepExecutor(cache, max_decode=D, max_tokens=T, max_chunks=D, max_blocks=P["max_blocks"])
+    stream = ex.stream
+    dt = pkv.torch_dtype(P["dtype"])
+    g = torch.Generator(device=device)
+    g.manual_seed(P["seed"] + rank)
+    dev_in = [torch.randn(shape, device=device, generator=g).to(dt)
+              for shape in ((L, D, n_q, d), (L, D, n_kv, d), (L, D, n_kv, d), (L, T, n_q, d), (L, T, n_kv, d),
+                            (L, T, n_kv, d))]
+    d_out = torch.empty((L, D, n_q, d), dtype=dt, device=device)
+    p_out = torch.empty((L, T, n_q, d), dtype=dt, device=device)
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=dt).pin_memory() for t in (d_out, p_out)]
+    scale = 1.0 / float(np.sqrt(d))
+    kv_tok = 2 * n_kv * d * 2
+
+    def one_run(copies: bool, timed_events: bool):
+        sched = Scheduler(cache.mgr, max_batch_tokens=T, chunk=P["chunk"], max_running=D, max_blocks=P["max_blocks"])
+        reqs = serve_trace(P)
+        evs, dec_bytes, pre_flops = [], [0], [0.0]
+        h2d, d2h = [0], [0]
+        t_start = [None]
+
+        def clock():
+            return time.perf_counter() - t_start[0]
+
+        def wait_until(t):
+            dt_ = t - clock()
+            if dt_ > 0:
+                time.sleep(dt_)
+
+        def on_kernel(kind, layer, when):
+            if not timed_events or kind != "decode":
+                return
+            if when == "start":
+                evs.append([torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)])
+                evs[-1][0].record(stream)
+            else:
+                evs[-1][1].record(stream)
+
+        def execute(plan):
+            nd, nt = plan.n_dec, plan.n_pre_tokens
+            dq, dk, dv, pq, pk, pv = dev_in
+            if copies:
+                with torch.cuda.stream(stream):
+                    for t_dev, t_host, n in zip(dev_in, host_in, (nd, nd, nd, nt, nt, nt)):
+                        if n:
+                            t_dev[:, :n].copy_(t_host[:, :n], non_blocking=True)
+                            h2d[0] += t_dev[:, :n].numel() * 2
+            ex.run(plan, (dq[:, :nd], dk[:, :nd], dv[:, :nd], d_out[:, :nd]),
+                   (pq[:, :nt], pk[:, :nt], pv[:, :nt], p_out[:, :nt]), scale, on_kernel)
+            if copies:
+                with torch.cuda.stream(stream):
+                    if nd:
+                        host_out[0][:, :nd].copy_(d_out[:, :nd], non_blocking=True)
+                        d2h[0] += d_out[:, :nd].numel() * 2
+                    if nt:
+                        host_out[1][:, :nt].copy_(p_out[:, :nt], non_blocking=True)
+                        d2h[0] += p_out[:, :nt].numel() * 2
+            stream.synchronize()                     # tokens of this iteration exist now
+            dec_bytes[0] += int(plan.dec_lens.astype(np.int64).sum()) * kv_tok * L
+            for i, (o, n) in enumerate(plan.pre_chunks):
+                c = int(plan.pre_lens[i])
+                pre_flops[0] += 4.0 * d * n_q * (n * (c - n) + n * (n + 1) / 2) * L
+
+        torch.cuda.synchronize()
+        barrier()
+        t_start[0] = time.perf_counter()
+        steps = serve(sched, reqs, execute, clock, wait_until)
+        wall = clock()
+        return sched, reqs, steps, wall, evs, dec_bytes[0], pre_flops[0], h2d[0], d2h[0]
+
+    # warm-up: a short trace (kernels loaded, tensor maps cached, pinned buffers touched)
+    saved = dict(P)
+    P.update(n_requests=max(8, args.warmup * 4))
+    for _ in range(1):
+        one_run(False, False)
+    P.clear()
+    P.update(saved)
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError("device status flags during warm-up")
+    sampler = ClockSampler(gpu_uuid(local))
+    sampler.start()
+    launches0 = pkv.pkv_launch_count()
+    sched, reqs, steps, wall, evs, dec_bytes, pre_flops, _, _ = one_run(False, True)
+    launches = pkv.pkv_launch_count() - launches0
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError("device status flags set during the timed run")
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs)
+    m = sched.metrics()
+    tokens = sum(r.generated for r in reqs if r.state == "done")
+    wall_max = reduce_over_ranks(wall, "max", device)
+    tokens_all = reduce_over_ranks(tokens, "sum", device)
+    sched2, reqs2, steps2, wall2, _, _, _, h2d, d2h = one_run(True, False)
+    wall2 = reduce_over_ranks(wall2, "max", device)
+    tokens2 = reduce_over_ranks(sum(r.generated for r in reqs2 if r.state == "done"), "sum", device)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": SERVE_METRIC, "value": round(tokens_all / wall_max, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(wall_max / max(steps, 1) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (Poisson arrivals; seeded q and K/V rows; no model weights)",
+        "config": {"workload": f"serve: {P['n_requests']} requests at {P['rate']}/s, 85% chat (prompt U{{64..512}}, "
+                               f"response min(Geom(1/500), 2048), priority 1) / 15% doc (prompt U{{2048..8192}}, "
+                               f"response U{{16..128}}, priority 0); GPT-style 32 layers x 32 heads x 128 fp16, "
+                               f"pool {P['num_blocks']} blocks ({P['num_blocks'] * 16} tokens)",
+                   "scheduler": f"max {T} tokens per iteration, prefill chunks <= {P['chunk']}, <= {D} running",
+                   "step": "one scheduler iteration (plan on the C manager, one metadata upload, CoW copies, per "
+                           "layer chunk append + prefill attention and fused append + decode attention, sync)",
+                   "l2": "no flush: decode iterations read more KV than L2 holds",
+                   "parallelism": f"replicas x{ws} (one trace per rank, no collective)"},
+        "wall_s": round(wall_max, 3),
+        "classes": m["classes"], "blocks": m["blocks"],
+        "prefill_tflops": round(pre_flops / wall / 1e12, 2),
+        "roofline": {"kernel": "paged_decode_mma_kernel (fused append) inside the serving loop", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "launch_ms_mean": round(dec_ms / max(1, len(evs)), 4),
+                     "algorithmic_bytes_per_launch": int(dec_bytes / max(1, len(evs)))},
+        "e2e": {"value": round(tokens2 / wall2, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d / max(steps2, 1)),
+                "d2h_bytes_per_step": int(d2h / max(steps2, 1)), "wall_s": round(wall2, 3)},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    return line
+
+
 def run_prefill_reference(args) -> dict | None:
     """Reference arm of the prefill line: the fp64 oracle, as it stands, on a bounded sample."""
     ws, rank, _ = dist_env()
@@ -750,7 +922,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="gpt", choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k"])
+    ap.add_argument("--config", default="gpt",
+                    choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k", "serve"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
@@ -761,9 +934,17 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
-        line = run_prefill_reference(args) if args.config == "prefill30k" else run_reference(args)
+        if args.config == "prefill30k":
+            line = run_prefill_reference(args)
+        elif args.config == "serve":
+            line = {"impl": "reference", "unavailable": "the serving loop has no CPU restatement: its kernels' "
+                                                       "reference arms are --config gpt and --config prefill30k"}
+        else:
+            line = run_reference(args)
     elif args.config == "prefill30k":
         line = run_prefill_gpu(args)
+    elif args.config == "serve":
+        line = run_serve_gpu(args)
     else:
         line = run_gpu(args)
     if line is not None:

@@ -391,9 +391,12 @@ class StepExecutor:
         m = st["np"]
         self._host(m, "dec_slots", np.int64)[:n_dec] = plan.dec_slots
         self._host(m, "pre_slots", np.int64)[:n_tok] = plan.pre_slots
-        self._host(m, "dec_tables")[: n_dec * self.mb] = plan.dec_tables.reshape(-1)
+        wd, wp = int(plan.dec_tables.shape[1]), int(plan.pre_tables.shape[1])
+        if wd > self.mb or wp > self.mb:
+            raise ValueError("plan tables wider than the executor's max_blocks")
+        self._host(m, "dec_tables")[: n_dec * wd] = plan.dec_tables.reshape(-1)
         self._host(m, "dec_lens")[:n_dec] = plan.dec_lens
-        self._host(m, "pre_tables")[: n_pre * self.mb] = plan.pre_tables.reshape(-1)
+        self._host(m, "pre_tables")[: n_pre * wp] = plan.pre_tables.reshape(-1)
         self._host(m, "pre_lens")[:n_pre] = plan.pre_lens
         self._host(m, "pre_qs")[: n_pre + 1] = plan.pre_qs
         self._host(m, "pairs")[: 2 * n_pairs] = plan.pairs.reshape(-1)
@@ -401,7 +404,7 @@ class StepExecutor:
             self.d_meta.copy_(st["meta"], non_blocking=True)
             st["done"].record(self.stream)
         st["used"] = True
-        return dict(n_dec=n_dec, n_pre=n_pre, n_tok=n_tok, n_pairs=n_pairs,
+        return dict(n_dec=n_dec, n_pre=n_pre, n_tok=n_tok, n_pairs=n_pairs, wd=wd, wp=wp,
                     max_q=max([n for _, n in plan.pre_chunks], default=0))
 
     def run(self, plan, dec_io, pre_io, scale: float, on_kernel=None) -> dict:
@@ -421,7 +424,7 @@ class StepExecutor:
                 if on_kernel is not None:
                     on_kernel("prefill", layer, "start")
                 pkv.pkv_paged_prefill_attention(
-                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * self.mb, (-1, self.mb)),
+                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * u["wp"], (-1, u["wp"])),
                     self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
                     stream=self.stream)
                 if on_kernel is not None:
@@ -432,7 +435,7 @@ class StepExecutor:
                     on_kernel("decode", layer, "start")
                 pkv.pkv_paged_decode_append_attention(
                     d, layer, q, k, v, c.k_pool, c.v_pool,
-                    self._dev("dec_tables", u["n_dec"] * self.mb, (-1, self.mb)), self._dev("dec_lens", u["n_dec"]),
+                    self._dev("dec_tables", u["n_dec"] * u["wd"], (-1, u["wd"])), self._dev("dec_lens", u["n_dec"]),
                     scale, out, self.workspace, stream=self.stream)
                 if on_kernel is not None:
                     on_kernel("decode", layer, "end")

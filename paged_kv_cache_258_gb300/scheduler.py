@@ -278,13 +278,18 @@ class Scheduler:
             pairs.append((src, dst))
         return True
 
+    def _width(self, ctxs) -> int:
+        """Table width of a plan: the longest context's blocks, rounded up to 16 entries (the
+        decode grid follows the width, so short iterations do not launch idle partitions)."""
+        need = max((math.ceil(c / self.bs) for c in ctxs), default=1)
+        return min(self.max_blocks, max(16, -(-need // 16) * 16))
+
     def _pack(self, dec, dec_slots, chunks, pairs, preempted) -> StepPlan:
-        mb = self.max_blocks
         dec_seq = np.array([r.seq for r in dec], dtype=np.int64)
-        rc, dec_tables, dec_lens = self.mgr.pack_tables(dec_seq, mb)
+        rc, dec_tables, dec_lens = self.mgr.pack_tables(dec_seq, self._width([r.cached + 1 for r in dec]))
         assert rc == pkv.PKV_OK
         pre_seq = np.array([o.seq for o, _ in chunks], dtype=np.int64)
-        rc, pre_tables, pre_lens = self.mgr.pack_tables(pre_seq, mb)
+        rc, pre_tables, pre_lens = self.mgr.pack_tables(pre_seq, self._width([o.cached + n for o, n in chunks]))
         assert rc == pkv.PKV_OK
         qs = np.zeros(len(chunks) + 1, dtype=np.int32)
         qs[1:] = np.cumsum([n for _, n in chunks]) if chunks else []
