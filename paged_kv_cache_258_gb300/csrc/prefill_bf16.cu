@@ -1,5 +1,5 @@
-// prefill_bf16.cu -- paged prefill attention instantiations for __nv_bfloat16 storage (tensor cores).
-#include "prefill_mma.cuh"
+// prefill_bf16.cu -- paged prefill attention instantiations (tcgen05 tensor cores) for __nv_bfloat16 storage.
+#include "prefill_umma.cuh"
 
 namespace pkv {
 
@@ -10,7 +10,7 @@ cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, c
     cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, &tk);
     if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, &tv);
     if (err != cudaSuccess) return err;
-    return launch_prefill_mma_dtype<__nv_bfloat16>(head_dim, group, a, tk, tv, stream);
+    return launch_prefill_umma_dtype<__nv_bfloat16>(head_dim, group, a, tk, tv, stream);
 }
 
 }  // namespace pkv
