@@ -6,18 +6,22 @@
 // sits at position c - n + i and attends to keys 0 .. that position through the block table.
 //
 // CTA = (128 query rows, KV head, sequence); rows = token x head-in-group (GQA rows packed, so each
-// K/V tile serves all G heads). Seven warps:
+// K/V tile serves all G heads). Tiles are BN = 128 keys (eight 16-token blocks): a tcgen05.mma costs
+// about the same at N = 64 as at N = 128, so S = Q K^T runs as N = 128 instructions. Seven warps:
 //   warps 0-3  softmax: thread t owns query row t, which is TMEM lane t (a warp reaches only its
-//              own 32 lanes); it reads its row of S, masks by selection, keeps the running max
-//              and sum in registers, writes its row of P (storage type) into shared memory;
-//   warps 4, 6 producers: walk the block table and move 64-key K tiles (warp 4) and V tiles
-//              (warp 6) of four 16-token blocks into a ring of ST stages with TMA tensor copies
-//              (128-byte swizzle); a K stage is released when S_j is done, a V stage when PV_j is;
-//              warp 6 zeroes the V rows of skipped blocks and of the positions past the context;
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers (128 x 64 fp32),
-//              then O += P_j V_j into a TMEM accumulator (128 x D fp32), each followed by a
-//              tcgen05.commit onto an mbarrier.
-// S is double-buffered, so S_{j+1} runs on the tensor pipe while the softmax warps work on S_j.
+//              own 32 lanes). It first writes its row of Q into TMEM (the A operand of S = Q K^T:
+//              no shared-memory reads of Q per instruction), then per tile reads its row of S,
+//              masks by selection, keeps the running max and sum in registers and writes its row
+//              of P (storage type) into shared memory;
+//   warps 4, 6 producers: walk the block table and move the K tiles (warp 4) and V tiles (warp 6)
+//              into rings of STK / STV stages with TMA tensor copies (128-byte swizzle); a K stage
+//              is released when S_j is done, a V stage when PV_j is; warp 6 zeroes the V rows of
+//              skipped blocks and of the positions past the context;
+//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of SB TMEM buffers (128 x BN fp32),
+//              then O += P_j V_j into a TMEM accumulator (128 x D fp32, one N = D instruction per
+//              16 keys), each followed by a tcgen05.commit onto an mbarrier.
+// S_{j+1} runs on the tensor pipe while the softmax warps work on S_j (they read S_j into registers
+// first and release its buffer).
 // O is rescaled (read, multiplied, written back in TMEM) only when a row's running maximum grows
 // by more than 8 (a factor 2^8 in the weights): P <= 2^8 stays exact enough in the storage type
 // and the final division by the same running sum keeps the result the softmax's. The weights are
@@ -48,22 +52,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 template <int D>
 struct UmmaTuning {
-    static constexpr int ST = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K/V stages
-    static constexpr int NP = D == 256 ? 1 : 2;                   // P buffers
-    static constexpr uint32_t TMEM_COLS = (128 + D) <= 256 ? 256u : 512u;
+    // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (a tcgen05.mma costs about
+    // the same time at N = 64 as at N = 128 on this part: small N wastes the tensor pipe).
+    static constexpr int BN = 128;
+    static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
+    static constexpr int STK = D == 64 ? 3 : 2;    // K stages
+    static constexpr int STV = D == 256 ? 1 : (D == 128 ? 2 : 3);  // V stages
+    static constexpr int NP = D == 256 ? 1 : 2;    // P buffers
+    // TMEM columns: S [0, SB*BN), O [SB*BN, SB*BN + D), Q [SB*BN + D, + D/2) (two 16-bit per column)
+    static constexpr uint32_t S_COL = 0, O_COL = SB * BN, Q_COL = SB * BN + D;
+    static constexpr uint32_t TMEM_COLS = (SB * BN + D + D / 2) <= 256 ? 256u : 512u;
+    static_assert(SB * BN + D + D / 2 <= 512, "tensor memory");
 };
 
-template <int D, int ST, int NP>
+template <int D>
 struct UmmaSmem {
-    static constexpr size_t QB = (size_t)128 * D * 2;   // Q [D/64][128 rows][128 B]
-    static constexpr size_t KT = (size_t)64 * D * 2;    // K or V tile [D/64][64 keys][128 B]
-    static constexpr size_t PB = (size_t)128 * 128;     // P [128 rows][64 keys x 2 B]
-    static constexpr size_t Q = 0;
-    static constexpr size_t KV = QB;                      // [ST][K tile, V tile]
-    static constexpr size_t P = KV + (size_t)ST * 2 * KT;
-    static constexpr size_t BARS = P + (size_t)NP * PB;
-    // full_k[ST] full_v[ST] k_empty[ST] v_empty[ST] s_full[2] s_free[2] p_full[NP] p_free[NP] vtail
-    static constexpr int NBARS = 4 * ST + 4 + 2 * NP + 1;
+    using Tu = UmmaTuning<D>;
+    static constexpr int BN = Tu::BN;
+    static constexpr size_t KT = (size_t)BN * D * 2;    // K or V tile [D/64][BN keys][128 B]
+    static constexpr size_t PB = (size_t)128 * BN * 2;  // P [BN/64][128 rows][128 B]
+    static constexpr size_t K = 0;                       // [STK] K tiles
+    static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V tiles
+    static constexpr size_t P = V + (size_t)Tu::STV * KT;  // [NP] P tiles
+    static constexpr size_t BARS = P + (size_t)Tu::NP * PB;
+    // full_k[STK] k_empty[STK] full_v[STV] v_empty[STV] s_full[SB] s_free[SB] p_full[NP] p_free[NP]
+    // vtail q_ready
+    static constexpr int NBARS = 2 * Tu::STK + 2 * Tu::STV + 2 * Tu::SB + 2 * Tu::NP + 2;
     static constexpr size_t TADDR = BARS + (size_t)NBARS * 8;  // TMEM base address
     static constexpr size_t TOTAL = TADDR + 16;
     static constexpr size_t ALLOC = TOTAL + 1024;
@@ -75,38 +89,36 @@ __global__ void __launch_bounds__(224, 1)
                               const __grid_constant__ CUtensorMap tm_v) {
     static_assert(128 % G == 0, "whole tokens per tile");
     using Tu = UmmaTuning<D>;
-    constexpr int ST = Tu::ST;
-    constexpr int NP = Tu::NP;
-    using S = UmmaSmem<D, ST, NP>;
+    using S = UmmaSmem<D>;
     using M = MmaType<T>;
+    constexpr int BN = Tu::BN, SB = Tu::SB, STK = Tu::STK, STV = Tu::STV, NP = Tu::NP;
+    constexpr int BPT = BN / kBlock;                    // blocks per tile
     constexpr int ROWS = 128;
     constexpr int QT = ROWS / G;
     constexpr int PANELS = D / 64;
     constexpr uint32_t KT = (uint32_t)S::KT;
-    constexpr uint32_t PANEL = 64 * 128;                // one 64-key panel of a K/V tile
+    constexpr uint32_t PANEL = BN * 128;                // one 64-column panel of a K/V tile
     constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int NPV = D > 128 ? 128 : D;             // N of one PV instruction
-    constexpr uint32_t IDESC_S = umma_idesc_f16(BF, 128, 64, false);
-    constexpr uint32_t IDESC_PV = umma_idesc_f16(BF, 128, NPV, true);
-    constexpr uint32_t S_COL = 0;                       // S buffers: columns [0, 128)
-    constexpr uint32_t O_COL = 128;                     // O: columns [128, 128 + D)
+    constexpr uint32_t IDESC_S = umma_idesc_f16(BF, 128, BN, false);
+    constexpr uint32_t IDESC_PV = umma_idesc_f16(BF, 128, D, true);
+    constexpr uint32_t S_COL = Tu::S_COL, O_COL = Tu::O_COL, Q_COL = Tu::Q_COL;
+    static_assert(BPT <= 32, "one lane per block of a tile");
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BARS);
-    uint64_t* full_k = bars;
-    uint64_t* full_v = full_k + ST;
-    uint64_t* k_empty = full_v + ST;
-    uint64_t* v_empty = k_empty + ST;
-    uint64_t* s_full = v_empty + ST;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
+    uint64_t* full_k = reinterpret_cast<uint64_t*>(smem + S::BARS);
+    uint64_t* k_empty = full_k + STK;
+    uint64_t* full_v = k_empty + STK;
+    uint64_t* v_empty = full_v + STV;
+    uint64_t* s_full = v_empty + STV;
+    uint64_t* s_free = s_full + SB;
+    uint64_t* p_full = s_free + SB;
     uint64_t* p_free = p_full + NP;
     uint64_t* vtail = p_free + NP;
+    uint64_t* q_ready = vtail + 1;
     uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::TADDR);
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t sQ = sbase + (uint32_t)S::Q;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -128,18 +140,20 @@ __global__ void __launch_bounds__(224, 1)
     const int t_end = min(t0 + QT, n_new);
     const int pos0 = ctx - n_new + t0;
     const int pos_last = ctx - n_new + t_end - 1;
-    const int n_tiles = pos_last / 64 + 1;
+    const int n_tiles = pos_last / BN + 1;      // BN-key tiles covering keys 0 .. pos_last
     const int nb = (ctx + kBlock - 1) / kBlock;
-    const bool tail_tile = n_tiles * 64 > ctx;
+    const bool tail_tile = n_tiles * BN > ctx;  // the last tile holds rows past the context
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < ST; ++i) {
+        for (int i = 0; i < STK; ++i) {
             mbar_init(&full_k[i], 1);
-            mbar_init(&full_v[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < STV; ++i) {
+            mbar_init(&full_v[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 128);
         }
@@ -148,22 +162,8 @@ __global__ void __launch_bounds__(224, 1)
             mbar_init(&p_free[i], 1);
         }
         mbar_init(vtail, 32);
+        mbar_init(q_ready, 128);
         fence_mbar_init();
-    }
-    // Q tile -> shared memory (128-byte swizzle, the layout tcgen05 reads); rows past the chunk are 0
-    {
-        const T* qg = reinterpret_cast<const T*>(a.q);
-        for (int i = threadIdx.x; i < ROWS * (D / 8); i += 224) {
-            const int r = i / (D / 8);
-            const int ch = i % (D / 8);
-            const int tt = r / G;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t0 + tt < n_new)
-                v = *reinterpret_cast<const uint4*>(qg + ((size_t)(q0 + t0 + tt) * a.n_q + (size_t)g * G + r % G) * D +
-                                                    ch * 8);
-            *reinterpret_cast<uint4*>(smem + S::Q + swzq<ROWS>(r, ch)) = v;
-        }
-        fence_proxy_async_smem();  // generic writes, read by the tensor core
     }
     if (warp == 5) tmem_alloc(taddr_s, Tu::TMEM_COLS);
     tcgen05_before_sync();
@@ -176,33 +176,35 @@ __global__ void __launch_bounds__(224, 1)
         // A K stage is released once S_j has been computed, a V stage once O += P_j V_j has: the next
         // K tile can land while the softmax of this one runs.
         const bool is_v = warp == 6;
+        const int nst = is_v ? STV : STK;
         uint64_t* full = is_v ? full_v : full_k;
         uint64_t* empty = is_v ? v_empty : k_empty;
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+        const uint32_t ring = (uint32_t)(is_v ? S::V : S::K);
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
         int issued = 0;
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % ST;
-            if (j >= ST && !mbar_wait_bounded(&empty[st], (uint32_t)((j / ST) - 1) & 1u)) {
+            const int st = j % nst;
+            if (j >= nst && !mbar_wait_bounded(&empty[st], (uint32_t)((j / nst) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                 break;
             }
-            const int blk = j * 4 + lane;
-            const bool inb = lane < 4 && blk < nb;
+            const int blk = j * BPT + lane;
+            const bool inb = lane < BPT && blk < nb;
             const int phys = inb ? trow[blk] : -1;
             const bool ok = inb && (unsigned)phys < (unsigned)a.num_blocks;
             const unsigned okm = __ballot_sync(0xffffffffu, ok);
             const unsigned badm = __ballot_sync(0xffffffffu, inb && !ok);
-            unsigned char* vst = smem + S::KV + (size_t)st * 2 * KT + KT;
+            unsigned char* tile_ptr = smem + ring + (size_t)st * KT;
             if (badm) {
                 // skipped blocks: keys masked by the softmax, V rows zeroed (P = 0 there, 0 * NaN is not)
                 if (!is_v && lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_BAD_BLOCK_ID);
                 if (is_v) {
-                    for (int b = 0; b < 4; ++b) {
+                    for (int b = 0; b < BPT; ++b) {
                         if (!((badm >> b) & 1u)) continue;
                         for (int i = lane; i < PANELS * 128; i += 32) {  // 2 KiB per panel = 128 x 16 B
                             const int pn = i / 128;
-                            reinterpret_cast<uint4*>(vst + (size_t)pn * PANEL + (size_t)b * 2048)[i % 128] =
+                            reinterpret_cast<uint4*>(tile_ptr + (size_t)pn * PANEL + (size_t)b * 2048)[i % 128] =
                                 make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
@@ -214,81 +216,74 @@ __global__ void __launch_bounds__(224, 1)
             __syncwarp();
             if (ok) {
                 const int row0 = (phys * a.n_kv + g) * kBlock;
-                const uint32_t dst = sbase + (uint32_t)S::KV + (uint32_t)st * 2 * KT + (is_v ? KT : 0u) +
-                                     (uint32_t)lane * 2048;
+                const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
 #pragma unroll
                 for (int pn = 0; pn < PANELS; ++pn) tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
             }
             issued = j + 1;
             if (is_v && j == n_tiles - 1 && tail_tile) {
-                if (!mbar_wait_bounded(&full_v[st], (uint32_t)(j / ST) & 1u)) {
+                if (!mbar_wait_bounded(&full_v[st], (uint32_t)(j / nst) & 1u)) {
                     if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                     break;
                 }
-                const int r0 = ctx - j * 64;  // first key row past the context, 1 .. 63
-                for (int i = lane; i < PANELS * (64 - r0) * 8; i += 32) {
-                    const int pn = i / ((64 - r0) * 8);
-                    const int rem = i % ((64 - r0) * 8);
-                    reinterpret_cast<uint4*>(vst + (size_t)pn * PANEL + (size_t)(r0 + rem / 8) * 128)[rem % 8] =
+                const int r0 = ctx - j * BN;  // first key row past the context, 1 .. BN-1
+                for (int i = lane; i < PANELS * (BN - r0) * 8; i += 32) {
+                    const int pn = i / ((BN - r0) * 8);
+                    const int rem = i % ((BN - r0) * 8);
+                    reinterpret_cast<uint4*>(tile_ptr + (size_t)pn * PANEL + (size_t)(r0 + rem / 8) * 128)[rem % 8] =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(vtail);
             }
         }
-        for (int j = max(0, issued - ST); j < issued; ++j)  // the copies of the last stages have landed
-            mbar_wait_bounded(&full[j % ST], (uint32_t)(j / ST) & 1u);
+        for (int j = max(0, issued - nst); j < issued; ++j)  // the copies of the last stages have landed
+            mbar_wait_bounded(&full[j % nst], (uint32_t)(j / nst) & 1u);
     } else if (warp == 5) {
         // ===================== MMA issuer =====================
         if (lane == 0) {
             bool ok = true;
             auto issue_s = [&](int j) -> bool {
-                const int st = j % ST;
-                const int b = j & 1;
-                if (!mbar_wait_bounded(&full_k[st], (uint32_t)(j / ST) & 1u)) return false;
-                if (j >= 2 && !mbar_wait_bounded(&s_free[b], (uint32_t)((j >> 1) - 1) & 1u)) return false;
+                const int st = j % STK;
+                const int b = j % SB;
+                if (!mbar_wait_bounded(&full_k[st], (uint32_t)(j / STK) & 1u)) return false;
+                if (j >= SB && !mbar_wait_bounded(&s_free[b], (uint32_t)((j / SB) - 1) & 1u)) return false;
                 tcgen05_after_sync();
-                const uint32_t sK = sbase + (uint32_t)S::KV + (uint32_t)st * 2 * KT;
+                const uint32_t sK = sbase + (uint32_t)S::K + (uint32_t)st * KT;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad = umma_desc_sw128(sQ + (uint32_t)(ks >> 2) * (ROWS * 128) + (uint32_t)(ks & 3) * 32,
-                                                        16, 1024);
                     const uint64_t bd = umma_desc_sw128(sK + (uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32, 16, 1024);
-                    umma_f16(tmem + S_COL + (uint32_t)b * 64, ad, bd, IDESC_S, ks > 0);
+                    umma_f16_tmem_a(tmem + S_COL + (uint32_t)(b * BN), tmem + Q_COL + (uint32_t)ks * 8, bd, IDESC_S, ks > 0);
                 }
                 umma_commit(&s_full[b]);
-                umma_commit(&k_empty[st]);  // the K stage may take tile j + ST once S_j is done
+                umma_commit(&k_empty[st]);  // the K stage may take tile j + STK once S_j is done
                 return true;
             };
-            ok = issue_s(0);
+            ok = mbar_wait_bounded(q_ready, 0u) && issue_s(0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !issue_s(j + 1)) {
                     ok = false;
                     break;
                 }
                 const int pb = j % NP;
-                const int st = j % ST;
+                const int sv = j % STV;
                 if (!mbar_wait_bounded(&p_full[pb], (uint32_t)(j / NP) & 1u) ||
-                    !mbar_wait_bounded(&full_v[st], (uint32_t)(j / ST) & 1u) ||
+                    !mbar_wait_bounded(&full_v[sv], (uint32_t)(j / STV) & 1u) ||
                     (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u))) {
                     ok = false;
                     break;
                 }
                 tcgen05_after_sync();
                 const uint32_t sP = sbase + (uint32_t)S::P + (uint32_t)pb * (uint32_t)S::PB;
-                const uint32_t sV = sbase + (uint32_t)S::KV + (uint32_t)st * 2 * KT + KT;
+                const uint32_t sV = sbase + (uint32_t)S::V + (uint32_t)sv * KT;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sP + (uint32_t)kk * 32, 16, 1024);
-#pragma unroll
-                    for (int h = 0; h < D / NPV; ++h) {
-                        const uint64_t bd = umma_desc_sw128(sV + (uint32_t)kk * 2048 + (uint32_t)h * (NPV / 64) * PANEL,
-                                                            PANEL, 1024);
-                        umma_f16(tmem + O_COL + (uint32_t)(h * NPV), ad, bd, IDESC_PV, j > 0 || kk > 0);
-                    }
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(sP + (uint32_t)(kk >> 2) * (128 * 128) + (uint32_t)(kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(sV + (uint32_t)kk * 2048, PANEL, 1024);
+                    umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
                 }
                 umma_commit(&p_free[pb]);
-                umma_commit(&v_empty[st]);
+                umma_commit(&v_empty[sv]);
             }
             if (!ok) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
             // every issued MMA has completed before TMEM is released (the last commit covers them all)
@@ -304,55 +299,73 @@ __global__ void __launch_bounds__(224, 1)
         const int lim = min(pos0 + tt, ctx - 1);
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float sl = a.scale_log2;
+        {
+            // this thread's query row -> TMEM lane `row` (the A operand of S = Q K^T); zero past the chunk
+            const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.q) +
+                                                               ((size_t)(q0 + t0 + tt) * a.n_q + (size_t)g * G + row % G) * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 w = live ? __ldg(qrow + c0 / 4 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    qv[4 * c] = w.x;
+                    qv[4 * c + 1] = w.y;
+                    qv[4 * c + 2] = w.z;
+                    qv[4 * c + 3] = w.w;
+                }
+                tmem_st32(tmem + lane_base + Q_COL + (uint32_t)c0, qv);
+            }
+            tmem_wait_st();
+            tcgen05_before_sync();
+            mbar_arrive(q_ready);
+        }
         float m_used = -INFINITY;
         float l = 0.f;
         bool ok = true;
-        unsigned char* prow_base = smem + S::P + (size_t)row * 128;
-        // which of a tile's four blocks were loaded (a table entry out of range is skipped): read from
-        // the table itself one tile ahead, so that no wait on a producer's barrier is needed here
+        // which of a tile's blocks were loaded (a table entry out of range is skipped): read from the
+        // table itself one tile ahead, so that no wait on a producer's barrier is needed here
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
-        auto tile_mask = [&](int j) -> int {
-            int m = 0;
+        auto tile_mask = [&](int j) -> unsigned {
+            unsigned m = 0;
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                const int blk = j * 4 + bb;
-                if (blk < nb && (unsigned)__ldg(trow + blk) < (unsigned)a.num_blocks) m |= 1 << bb;
+            for (int bb = 0; bb < BPT; ++bb) {
+                const int blk = j * BPT + bb;
+                if (blk < nb && (unsigned)__ldg(trow + blk) < (unsigned)a.num_blocks) m |= 1u << bb;
             }
             return m;
         };
-        int okm_next = tile_mask(0);
+        constexpr unsigned FULL = (1u << BPT) - 1u;
+        unsigned okm_next = tile_mask(0);
         for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
+            const int b = j % SB;
             const int pb = j % NP;
-            const int okm = okm_next;
+            const unsigned okm = okm_next;
             if (j + 1 < n_tiles) okm_next = tile_mask(j + 1);
-            if (!mbar_wait_bounded(&s_full[b], (uint32_t)(j >> 1) & 1u)) {
+            if (!mbar_wait_bounded(&s_full[b], (uint32_t)(j / SB) & 1u)) {
                 ok = false;
                 break;
             }
             tcgen05_after_sync();
-            uint32_t sv[64];
-            tmem_ld32(tmem + lane_base + S_COL + (uint32_t)b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(tmem + lane_base + S_COL + (uint32_t)b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            float sc[BN];
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32)
+                tmem_ld32(tmem + lane_base + S_COL + (uint32_t)(b * BN + c0), *reinterpret_cast<uint32_t(*)[32]>(&sc[c0]));
             tmem_wait_ld();
             tcgen05_before_sync();
-            mbar_arrive(&s_free[b]);  // the S buffer may take S_{j+2}
-            const int key0 = j * 64;
-            float sc[64];
+            mbar_arrive(&s_free[b]);  // the S buffer may take S_{j+SB}
+            const int key0 = j * BN;
             float mx8[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) mx8[c] = -INFINITY;
-            if (key0 + 63 <= lim && okm == 0xF) {
+            if (key0 + BN - 1 <= lim && okm == FULL) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    sc[c] = __uint_as_float(sv[c]);
-                    mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
-                }
+                for (int c = 0; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
             } else {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {  // masking by selection: a masked score is -inf
-                    const bool v = key0 + c <= lim && ((okm >> (c >> 4)) & 1);
-                    sc[c] = v ? __uint_as_float(sv[c]) : -INFINITY;
+                for (int c = 0; c < BN; ++c) {  // masking by selection: a masked score is -inf
+                    const bool v = key0 + c <= lim && ((okm >> (c >> 4)) & 1u);
+                    sc[c] = v ? sc[c] : -INFINITY;
                     mx8[c & 7] = fmaxf(mx8[c & 7], sc[c]);
                 }
             }
@@ -386,12 +399,12 @@ __global__ void __launch_bounds__(224, 1)
             // p = 2^(s * scale_log2 - m): one FFMA and one ex2 per score; a masked score (-inf) gives
             // exactly 0. While every score so far is masked m_used is -inf: subtract 0 instead.
             const float msub = m_used == -INFINITY ? 0.f : m_used;
-            uint32_t pw[32];
+            uint32_t pw[BN / 2];
             float ls[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) ls[c] = 0.f;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < BN / 2; ++c) {
                 const float p0 = ex2_approx(fmaf(sc[2 * c], sl, -msub));
                 const float p1 = ex2_approx(fmaf(sc[2 * c + 1], sl, -msub));
                 pw[c] = M::pack(p0, p1);
@@ -403,11 +416,14 @@ __global__ void __launch_bounds__(224, 1)
                 ok = false;
                 break;
             }
-            unsigned char* prow = prow_base + (size_t)pb * S::PB;
+            unsigned char* prow = smem + S::P + (size_t)pb * S::PB + (size_t)row * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-                    make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            for (int pp = 0; pp < BN / 64; ++pp)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(prow + (size_t)pp * (128 * 128) + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(pw[32 * pp + 4 * c], pw[32 * pp + 4 * c + 1], pw[32 * pp + 4 * c + 2],
+                                   pw[32 * pp + 4 * c + 3]);
             fence_proxy_async_smem();
             tcgen05_before_sync();
             mbar_arrive(&p_full[pb]);
@@ -451,8 +467,7 @@ __global__ void __launch_bounds__(224, 1)
 template <typename T, int D, int G>
 cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                     cudaStream_t stream) {
-    using Tu = UmmaTuning<D>;
-    constexpr size_t smem = UmmaSmem<D, Tu::ST, Tu::NP>::ALLOC;
+    constexpr size_t smem = UmmaSmem<D>::ALLOC;
     static_assert(smem <= 227 * 1024, "shared memory per CTA");
     auto kern = paged_prefill_umma_kernel<T, D, G>;
     int dev = 0;
