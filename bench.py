@@ -395,6 +395,34 @@ def prefill_chunks(prompt: int, chunk: int):
     return [(c0, min(chunk, prompt - c0)) for c0 in range(0, prompt, chunk)]
 
 
+def setup_prefill_case(device, rank: int = 0, layers=None, placement: str = "shuffled"):
+    """The prefill30k case as bench.py times it: pools, chunk stepper and resident inputs."""
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+    from paged_kv_cache_258_gb300.engine import PagedKVCache, PrefillStep
+    P = dict(PREFILL)
+    if layers:
+        P["n_layers"] = layers
+    L, n_q, n_kv, d, prompt, chunk = P["n_layers"], P["n_q"], P["n_kv"], P["d"], P["prompt"], P["chunk"]
+    seed = W.BASE_SEED + 5 + rank
+    P["seed"] = seed
+    nb_seq = -(-prompt // W.BLOCK)
+    num_blocks = int(nb_seq * 1.125) + 1
+    desc = pkv.make_desc(P["dtype"], L, num_blocks, n_q, n_kv, d)
+    order = W.free_order(num_blocks, seed) if placement == "shuffled" else None
+    P["free_order"] = order
+    cache = PagedKVCache(desc, free_order=order, device=device)
+    ps = PrefillStep(cache, max_tokens=chunk, max_seqs=1, max_blocks=nb_seq)
+    dt = pkv.torch_dtype(P["dtype"])
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = torch.randn((L, prompt, n_q, d), device=device, generator=g).to(dt)
+    k_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
+    v_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
+    out = torch.empty_like(q)
+    return P, cache, ps, (q, k_new, v_new, out), prefill_chunks(prompt, chunk)
+
+
 def run_prefill_gpu(args) -> dict | None:
     import torch
     from paged_kv_cache_258_gb300 import pkv
@@ -404,27 +432,11 @@ def run_prefill_gpu(args) -> dict | None:
     _, _, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    P = dict(PREFILL)
-    if args.layers:
-        P["n_layers"] = args.layers
+    pkv.lib()
+    P, cache, ps, (q, k_new, v_new, out), chunks = setup_prefill_case(device, rank, args.layers, args.placement)
     L, n_q, n_kv, d, prompt, chunk = P["n_layers"], P["n_q"], P["n_kv"], P["d"], P["prompt"], P["chunk"]
-    seed = W.BASE_SEED + 5 + rank
-    nb_seq = -(-prompt // W.BLOCK)
-    num_blocks = int(nb_seq * 1.125) + 1
-    desc = pkv.make_desc(P["dtype"], L, num_blocks, n_q, n_kv, d)
-    order = W.free_order(num_blocks, seed) if args.placement == "shuffled" else None
-    cache = PagedKVCache(desc, free_order=order, device=device)
-    ps = PrefillStep(cache, max_tokens=chunk, max_seqs=1, max_blocks=nb_seq)
     stream = ps.stream
-    dt = pkv.torch_dtype(P["dtype"])
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    q = torch.randn((L, prompt, n_q, d), device=device, generator=g).to(dt)
-    k_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
-    v_new = torch.randn((L, prompt, n_kv, d), device=device, generator=g).to(dt)
-    out = torch.empty_like(q)
     scale = 1.0 / float(np.sqrt(d))
-    chunks = prefill_chunks(prompt, chunk)
     seq = 1
 
     def one_step(on_attn=None, bufs=None):
@@ -526,7 +538,7 @@ def run_prefill_gpu(args) -> dict | None:
                    "parallelism": f"replicas x{ws} (one prompt per rank, no collective)",
                    "placement": args.placement},
         "prompt_tokens_per_s": round(prompt * args.steps * ws / (ms * 1e-3), 1),
-        "roofline": {"kernel": "paged_prefill_mma_kernel (mma.sync m16n8k16, TMA producer warp)",
+        "roofline": {"kernel": "paged_prefill_umma_kernel (tcgen05, S and O in tensor memory, TMA K/V producers)",
                      "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "launch_ms_mean": round(attn_ms / n_launch, 4),
@@ -539,7 +551,7 @@ def run_prefill_gpu(args) -> dict | None:
         "clocks": clocks,
     }
     if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = prefill_cpu_sample(cache, budget_s=args.cpu_budget, P=P, seed=seed)
+        line["cpu_baseline"] = prefill_cpu_sample(cache, budget_s=args.cpu_budget, P=P, seed=P["seed"])
     return line
 
 

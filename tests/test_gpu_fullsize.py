@@ -62,3 +62,43 @@ def test_fullsize_sampled(config, layers, seqs):
         assert err <= TOL[dtype], f"{config} layer {l}: max abs error {err:.3e}"
     # every output row of the step is finite
     assert torch.isfinite(out.float()).all()
+
+
+def test_prefill30k_fullsize_sampled():
+    """The 30,000-token prompt of the prefill30k line, chunked exactly as bench.py runs it (2 of its
+    16 layers: every launch is identical per layer), sampled query positions of every chunk checked
+    against the oracle one query at a time. The oracle's pools are its own byte appends of the
+    generated rows at the slots of its own block-manager replay (add_seq for the first chunk,
+    extend for the others)."""
+    device = torch.device("cuda", 0)
+    P, cache, ps, (q, kn, vn, out), chunks = bench.setup_prefill_case(device, layers=2)
+    dtype, L, d = P["dtype"], P["n_layers"], P["d"]
+    scale = 1.0 / np.sqrt(d)
+    mo = BlockManagerOracle(cache.desc.num_blocks, free_order=P["free_order"])
+    nb = cache.desc.num_blocks
+    host_k = np.zeros((L, nb, P["n_kv"], 16, d), np.uint16)
+    host_v = np.zeros_like(host_k)
+    kn_h, vn_h, q_h = to_host(kn, dtype), to_host(vn, dtype), to_host(q, dtype)
+    for i, (c0, n) in enumerate(chunks):
+        st = ps.step([(1, n, i == 0)], q[:, c0:c0 + n], kn[:, c0:c0 + n], vn[:, c0:c0 + n], out[:, c0:c0 + n],
+                     scale)
+        s_, slots = mo.add_seq(1, n) if i == 0 else mo.extend(1, n)[:2]
+        assert s_ == "ok"
+        assert st["np"][: 2 * ps.max_tokens].view(np.int64)[:n].tolist() == list(slots)
+        for layer in range(L):
+            oracle.kv_append(kn_h[layer, c0:c0 + n], vn_h[layer, c0:c0 + n], np.array(slots), host_k[layer],
+                             host_v[layer])
+    assert pkv.pkv_get_device_status() == 0
+    t, ctx = mo.block_table(1)
+    assert ctx == P["prompt"]
+    # sampled positions: first, middle and last token of every chunk, plus the prompt's last token
+    pos = sorted({p for c0, n in chunks for p in (c0, c0 + n // 2, c0 + n - 1)})
+    tables = np.tile(np.array(t, dtype=np.int32), (len(pos), 1))
+    lens = np.array(pos, dtype=np.int32) + 1          # each sample: one query at its own position
+    qs = np.arange(len(pos) + 1, dtype=np.int32)
+    got = as_f64(out)
+    for layer in range(L):
+        want = oracle.paged_prefill(dtype, q_h[layer, pos], host_k[layer], host_v[layer], tables, lens, qs, scale,
+                                    n_threads=oracle.max_threads())
+        err = np.max(np.abs(got[layer, pos] - want))
+        assert err <= TOL[dtype], f"layer {layer}: {err:.3e}"
