@@ -53,10 +53,8 @@ struct PrefillArgs {
 
 // Query rows (token x head-in-group) one prefill CTA covers; tokens per CTA = rows / group.
 // tcgen05 kernel (fp16 / bf16): 128 rows, the M of one tensor-core instruction (one TMEM lane per
-// row). mma.sync kernel (kept for comparison): 16 rows per consumer warp, 8 warps (7 at head_dim
-// 256 so that a thread may hold 255 registers). CUDA-core kernel (fp32): 32 rows.
+// row). CUDA-core kernel (fp32): 32 rows.
 constexpr int kPrefillRowsUmma = 128;
-constexpr int prefill_mma_rows(int head_dim) { return head_dim == 256 ? 112 : 128; }
 constexpr int kPrefillRowsF32 = 32;
 inline int prefill_tokens_per_cta(int dtype, int head_dim, int group) {
     (void)head_dim;

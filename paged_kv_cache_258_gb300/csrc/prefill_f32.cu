@@ -1,7 +1,7 @@
 // prefill_f32.cu -- paged prefill attention for fp32 storage on the CUDA cores, and the dtype
 // dispatch of all prefill launches.
 //
-// Same operation as prefill_mma.cuh ("PagedAttention e continuous batching", "01 - Conceito",
+// Same operation as prefill_umma.cuh ("PagedAttention e continuous batching", "01 - Conceito",
 // paragraph 5; "La idea de PagedAttention", step 5): chunk token i of sequence s sits at
 // position c - n + i and attends to keys 0 .. that position, gathered through the block table.
 // fp32 storage is the precision mode (1e-5 against the fp64 oracle), which tf32 tensor cores

@@ -1,9 +1,12 @@
 // prefill_umma.cuh -- paged prefill / chunked prefill attention on the tcgen05 tensor cores (fp16 /
 // bf16), accumulators in tensor memory.
 //
-// Same operation and masking rules as prefill_mma.cuh ("PagedAttention e continuous batching",
-// "01 - Conceito", paragraph 5; "La idea de PagedAttention", step 5): chunk token i of sequence s
-// sits at position c - n + i and attends to keys 0 .. that position through the block table.
+// A chunk of n new tokens per sequence attends causally to the sequence's cache through its block
+// table ("PagedAttention e continuous batching", "01 - Conceito", paragraph 5: long prompts are
+// sliced into chunks; "04 - Hacia PagedAttention (vista previa)", "La idea de PagedAttention",
+// step 5: the kernel gathers the rows itself). The chunk's tokens are the newest, already
+// appended: with c = context_lens[s] they sit at positions c - n .. c - 1, and position p sees keys
+// 0 .. p. Unlike decode this is a dense contraction (n query rows x c keys x head_dim).
 //
 // CTA = (128 query rows, KV head, sequence); rows = token x head-in-group (GQA rows packed, so each
 // K/V tile serves all G heads). Tiles are BN = 128 keys (eight 16-token blocks): a tcgen05.mma costs
@@ -38,10 +41,19 @@
 #include "common.cuh"
 #include "decode_mma.cuh"
 #include "internal.h"
-#include "prefill_mma.cuh"
 #include "umma.cuh"
 
 namespace pkv {
+
+// 2-D tensor copy of a 64-column x 16-row box with the default L2 policy (the K/V tiles of a prefill
+// are re-read by every query tile of the sequence, so they should stay in L2).
+__device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
 
 // 2^x with the ex2.approx.ftz instruction (2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
