@@ -15,7 +15,8 @@
 //              own 32 lanes). It first writes its row of Q into TMEM (the A operand of S = Q K^T:
 //              no shared-memory reads of Q per instruction), then per tile reads its row of S,
 //              masks by selection, keeps the running max and sum in registers and writes its row
-//              of P (storage type) into shared memory;
+//              of P (storage type) into TMEM (d <= 128) or shared memory (d = 256, where TMEM is
+//              full: S 128 + O 256 + Q 128 columns);
 //   warps 4, 6 producers: walk the block table and move the K tiles (warp 4) and V tiles (warp 6)
 //              into rings of STK / STV stages with TMA tensor copies (128-byte swizzle); a K stage
 //              is released when S_j is done, a V stage when PV_j is; warp 6 zeroes the V rows of
@@ -67,14 +68,17 @@ struct UmmaTuning {
     // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (a tcgen05.mma costs about
     // the same time at N = 64 as at N = 128 on this part: small N wastes the tensor pipe).
     static constexpr int BN = 128;
+    static constexpr bool PT = D <= 128;          // P in TMEM (A operand of PV) rather than shared memory
     static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
-    static constexpr int STK = D == 64 ? 3 : 2;    // K stages
-    static constexpr int STV = D == 256 ? 1 : (D == 128 ? 2 : 3);  // V stages
-    static constexpr int NP = D == 256 ? 1 : 2;    // P buffers
-    // TMEM columns: S [0, SB*BN), O [SB*BN, SB*BN + D), Q [SB*BN + D, + D/2) (two 16-bit per column)
-    static constexpr uint32_t S_COL = 0, O_COL = SB * BN, Q_COL = SB * BN + D;
-    static constexpr uint32_t TMEM_COLS = (SB * BN + D + D / 2) <= 256 ? 256u : 512u;
-    static_assert(SB * BN + D + D / 2 <= 512, "tensor memory");
+    static constexpr int STK = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K stages
+    static constexpr int STV = D == 256 ? 1 : (D == 128 ? 3 : 4);  // V stages
+    static constexpr int NP = D == 64 ? 2 : 1;     // P buffers
+    // TMEM columns: S [0, SB*BN), O [SB*BN, +D), Q [.., +D/2), P [.., +NP*BN/2) when PT (16-bit
+    // operands hold two elements per 32-bit column)
+    static constexpr uint32_t S_COL = 0, O_COL = SB * BN, Q_COL = SB * BN + D, P_COL = Q_COL + D / 2;
+    static constexpr uint32_t USED = P_COL + (PT ? NP * BN / 2 : 0);
+    static constexpr uint32_t TMEM_COLS = USED <= 256 ? 256u : 512u;
+    static_assert(USED <= 512, "tensor memory");
 };
 
 template <int D>
@@ -82,7 +86,7 @@ struct UmmaSmem {
     using Tu = UmmaTuning<D>;
     static constexpr int BN = Tu::BN;
     static constexpr size_t KT = (size_t)BN * D * 2;    // K or V tile [D/64][BN keys][128 B]
-    static constexpr size_t PB = (size_t)128 * BN * 2;  // P [BN/64][128 rows][128 B]
+    static constexpr size_t PB = Tu::PT ? 0 : (size_t)128 * BN * 2;  // P [BN/64][128 rows][128 B]
     static constexpr size_t K = 0;                       // [STK] K tiles
     static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V tiles
     static constexpr size_t P = V + (size_t)Tu::STV * KT;  // [NP] P tiles
@@ -290,9 +294,15 @@ __global__ void __launch_bounds__(224, 1)
                 const uint32_t sV = sbase + (uint32_t)S::V + (uint32_t)sv * KT;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(sP + (uint32_t)(kk >> 2) * (128 * 128) + (uint32_t)(kk & 3) * 32, 16, 1024);
                     const uint64_t bd = umma_desc_sw128(sV + (uint32_t)kk * 2048, PANEL, 1024);
-                    umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                    if constexpr (Tu::PT) {
+                        umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd, IDESC_PV,
+                                        j > 0 || kk > 0);
+                    } else {
+                        const uint64_t ad =
+                            umma_desc_sw128(sP + (uint32_t)(kk >> 2) * (128 * 128) + (uint32_t)(kk & 3) * 32, 16, 1024);
+                        umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                    }
                 }
                 umma_commit(&p_free[pb]);
                 umma_commit(&v_empty[sv]);
@@ -428,15 +438,25 @@ __global__ void __launch_bounds__(224, 1)
                 ok = false;
                 break;
             }
-            unsigned char* prow = smem + S::P + (size_t)pb * S::PB + (size_t)row * 128;
+            if constexpr (Tu::PT) {
+                // this row of P -> TMEM lane `row`, two 16-bit weights per column
+                if (j >= NP) tcgen05_after_sync();
 #pragma unroll
-            for (int pp = 0; pp < BN / 64; ++pp)
+                for (int c0 = 0; c0 < BN / 2; c0 += 32)
+                    tmem_st32(tmem + lane_base + Tu::P_COL + (uint32_t)(pb * (BN / 2) + c0),
+                              *reinterpret_cast<const uint32_t(*)[32]>(&pw[c0]));
+                tmem_wait_st();
+            } else {
+                unsigned char* prow = smem + S::P + (size_t)pb * S::PB + (size_t)row * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + (size_t)pp * (128 * 128) + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(pw[32 * pp + 4 * c], pw[32 * pp + 4 * c + 1], pw[32 * pp + 4 * c + 2],
-                                   pw[32 * pp + 4 * c + 3]);
-            fence_proxy_async_smem();
+                for (int pp = 0; pp < BN / 64; ++pp)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(prow + (size_t)pp * (128 * 128) + ((c ^ (row & 7)) << 4)) =
+                            make_uint4(pw[32 * pp + 4 * c], pw[32 * pp + 4 * c + 1], pw[32 * pp + 4 * c + 2],
+                                       pw[32 * pp + 4 * c + 3]);
+                fence_proxy_async_smem();
+            }
             tcgen05_before_sync();
             mbar_arrive(&p_full[pb]);
         }
