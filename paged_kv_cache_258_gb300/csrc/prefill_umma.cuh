@@ -56,6 +56,17 @@ __device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// The same copy delivered to the same shared-memory offset, and its bytes signalled to the mbarrier
+// at the same offset, in every CTA of `cta_mask` (one L2 read feeds several SMs).
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // 2^x with the ex2.approx.ftz instruction (2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -68,6 +79,10 @@ struct UmmaTuning {
     // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (a tcgen05.mma costs about
     // the same time at N = 64 as at N = 128 on this part: small N wastes the tensor pipe).
     static constexpr int BN = 128;
+    // CTAs per cluster sharing K/V loads: at head_dim 256 every CTA would pull 128 KiB per 128-key
+    // tile from L2 (the measured limit), so two CTAs with adjacent query tiles of the same sequence
+    // and KV head each load half of every common tile and multicast it to both.
+    static constexpr int CL = D == 256 ? 2 : 1;
     static constexpr bool PT = D <= 128;          // P in TMEM (A operand of PV) rather than shared memory
     static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
     static constexpr int STK = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K stages
@@ -136,6 +151,7 @@ __global__ void __launch_bounds__(224, 1)
     uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::TADDR);
     const uint32_t sbase = smem_addr(smem);
 
+    constexpr int CL = Tu::CL;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int tile = a.q_tiles - 1 - (int)blockIdx.x;  // tiles with the most keys start first
@@ -146,28 +162,41 @@ __global__ void __launch_bounds__(224, 1)
     const int q1 = a.q_start[s + 1];
     const int n_new = q1 - q0;
     const int ctx = a.lens[s];
-    if (q0 < 0 || q1 > a.n_tokens || n_new < 0 || n_new > a.q_tiles * QT || ctx < n_new ||
-        ctx > a.max_blocks * kBlock) {
-        if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0) atomicOr(a.status, (unsigned)PKV_DEV_BAD_QUERY_RANGE);
+    const bool bad = q0 < 0 || q1 > a.n_tokens || n_new < 0 || n_new > a.q_tiles * QT || ctx < n_new ||
+                     ctx > a.max_blocks * kBlock;
+    if (bad && blockIdx.x == 0 && g == 0 && threadIdx.x == 0) atomicOr(a.status, (unsigned)PKV_DEV_BAD_QUERY_RANGE);
+    // BN-key tiles a query tile needs: keys 0 .. the position of its last token (0: no rows)
+    auto key_tiles = [&](int qt) -> int {
+        const int tq0 = qt * QT;
+        if (bad || qt < 0 || tq0 >= n_new) return 0;
+        return (ctx - n_new + min(tq0 + QT, n_new) - 1) / BN + 1;
+    };
+    const int n_tiles = key_tiles(tile);
+    // tiles shared with the other CTA of the cluster (same sequence and KV head, adjacent query tile)
+    const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+    const int n_common = CL > 1 ? min(n_tiles, key_tiles(a.q_tiles - 1 - (int)(blockIdx.x ^ 1u))) : 0;
+    if (n_tiles == 0) {
+        if constexpr (CL > 1) {  // still meet the other CTA at its two cluster barriers
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
     const int t0 = tile * QT;
-    if (t0 >= n_new) return;
-    const int t_end = min(t0 + QT, n_new);
     const int pos0 = ctx - n_new + t0;
-    const int pos_last = ctx - n_new + t_end - 1;
-    const int n_tiles = pos_last / BN + 1;      // BN-key tiles covering keys 0 .. pos_last
     const int nb = (ctx + kBlock - 1) / kBlock;
     const bool tail_tile = n_tiles * BN > ctx;  // the last tile holds rows past the context
 
     if (threadIdx.x == 0) {
+        // a stage is free again when the MMAs of every CTA that reads it are done with it: CL
+        // arrivals (the other CTA's by multicast commit; twice this CTA's for a tile only it reads)
         for (int i = 0; i < STK; ++i) {
             mbar_init(&full_k[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], CL);
         }
         for (int i = 0; i < STV; ++i) {
             mbar_init(&full_v[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], CL);
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
@@ -184,6 +213,7 @@ __global__ void __launch_bounds__(224, 1)
     if (warp == 5) tmem_alloc(taddr_s, Tu::TMEM_COLS);
     tcgen05_before_sync();
     __syncthreads();
+    if constexpr (CL > 1) cluster_sync_all();  // the other CTA's mbarriers exist before any multicast
     tcgen05_after_sync();
     const uint32_t tmem = *taddr_s;
 
@@ -233,8 +263,17 @@ __global__ void __launch_bounds__(224, 1)
             if (ok) {
                 const int row0 = (phys * a.n_kv + g) * kBlock;
                 const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
+                if (CL > 1 && j < n_common) {
+                    // common tile: this CTA loads its share of the blocks into every CTA of the cluster
+                    if ((uint32_t)lane * CL / BPT == crank) {
 #pragma unroll
-                for (int pn = 0; pn < PANELS; ++pn) tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
+                        for (int pn = 0; pn < PANELS; ++pn)
+                            tma_load_2d_multicast(dst + pn * PANEL, tm, pn * 64, row0, &full[st], (uint16_t)((1u << CL) - 1u));
+                    }
+                } else {
+#pragma unroll
+                    for (int pn = 0; pn < PANELS; ++pn) tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
+                }
             }
             issued = j + 1;
             if (is_v && j == n_tiles - 1 && tail_tile) {
@@ -259,6 +298,16 @@ __global__ void __launch_bounds__(224, 1)
         // ===================== MMA issuer =====================
         if (lane == 0) {
             bool ok = true;
+            // a stage of a common tile is released in every CTA of the cluster; a stage only this
+            // CTA reads gets all CL arrivals from here
+            auto release = [&](uint64_t* bar, int j) {
+                if (CL > 1 && j < n_common) {
+                    umma_commit_multicast(bar, (uint16_t)((1u << CL) - 1u));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < CL; ++c) umma_commit(bar);
+                }
+            };
             auto issue_s = [&](int j) -> bool {
                 const int st = j % STK;
                 const int b = j % SB;
@@ -272,7 +321,7 @@ __global__ void __launch_bounds__(224, 1)
                     umma_f16_tmem_a(tmem + S_COL + (uint32_t)(b * BN), tmem + Q_COL + (uint32_t)ks * 8, bd, IDESC_S, ks > 0);
                 }
                 umma_commit(&s_full[b]);
-                umma_commit(&k_empty[st]);  // the K stage may take tile j + STK once S_j is done
+                release(k_empty + st, j);  // the K stage may take tile j + STK once S_j is done
                 return true;
             };
             ok = mbar_wait_bounded(q_ready, 0u) && issue_s(0);
@@ -305,12 +354,24 @@ __global__ void __launch_bounds__(224, 1)
                     }
                 }
                 umma_commit(&p_free[pb]);
-                umma_commit(&v_empty[sv]);
+                release(v_empty + sv, j);
             }
             if (!ok) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
             // every issued MMA has completed before TMEM is released (the last commit covers them all)
             const int last = n_tiles - 1;
             mbar_wait_bounded(&p_free[last % NP], (uint32_t)(last / NP) & 1u);
+            if constexpr (CL > 1) {
+                // and every release the other CTA sends here has landed: the last phase of each stage
+                // completes only with all of its arrivals
+                for (int st = 0; st < STK && st < n_tiles; ++st) {
+                    const int jl = st + ((n_tiles - 1 - st) / STK) * STK;
+                    mbar_wait_bounded(&k_empty[st], (uint32_t)(jl / STK) & 1u);
+                }
+                for (int st = 0; st < STV && st < n_tiles; ++st) {
+                    const int jl = st + ((n_tiles - 1 - st) / STV) * STV;
+                    mbar_wait_bounded(&v_empty[st], (uint32_t)(jl / STV) & 1u);
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -490,6 +551,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     tcgen05_before_sync();
     __syncthreads();
+    if constexpr (CL > 1) cluster_sync_all();  // no CTA leaves while the other may still write to it
     if (warp == 5) {
         tcgen05_after_sync();
         tmem_dealloc(tmem, Tu::TMEM_COLS);
@@ -511,8 +573,23 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    dim3 grid(a.q_tiles, a.n_kv, a.n_seqs);
-    kern<<<grid, 224, smem, stream>>>(a, tk, tv);
+    constexpr int CL = UmmaTuning<D>::CL;
+    PrefillArgs b = a;
+    b.q_tiles = (a.q_tiles + CL - 1) / CL * CL;  // whole clusters; the extra query tiles have no rows
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(b.q_tiles, b.n_kv, b.n_seqs);
+    cfg.blockDim = dim3(224, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, b, tk, tv);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
