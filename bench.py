@@ -765,6 +765,8 @@ def run_serve_gpu(args) -> dict | None:
     P = dict(SERVE)
     if args.layers:
         P["n_layers"] = args.layers
+    if args.rate:
+        P["rate"] = float(args.rate)
     L, n_q, n_kv, d = P["n_layers"], P["n_q"], P["n_kv"], P["d"]
     desc = pkv.make_desc(P["dtype"], L, P["num_blocks"], n_q, n_kv, d)
     order = W.free_order(P["num_blocks"], P["seed"] + rank)
@@ -942,6 +944,8 @@ def main(argv=None):
     ap.add_argument("--placement", default="shuffled", choices=["shuffled", "contiguous"],
                     help="physical placement of each sequence's blocks (indirection-overhead study)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--rate", type=float, default=None,
+                    help="serve: request arrivals per second (default 48; a very large rate submits all at once)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -263,6 +263,15 @@ int pkv_get_device_status(void* stream, uint32_t* flags);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t pkv_launch_count(void);
 
+/*
+ * Self-test of the bounded waits every kernel here uses on its asynchronous copies: launches one
+ * CTA that waits on an mbarrier nothing will ever complete. The wait gives up after its limit
+ * (about one second), records PKV_DEV_WAIT_TIMEOUT in the device status word (read it with
+ * pkv_get_device_status) and the kernel returns normally, leaving the context usable. No fault,
+ * trap or hang is involved. Asynchronous on `stream`; PKV_ERR_CUDA if the launch fails.
+ */
+int pkv_selftest_wait_timeout(void* stream);
+
 /* ---- host block manager ------------------------------------------------------------ */
 
 typedef struct pkv_mgr pkv_mgr;

@@ -2,12 +2,22 @@
 #include <atomic>
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace {
 
 // Device status word: kernels OR PKV_DEV_* bits into it when they skip a bad device-side value.
 __device__ unsigned int g_dev_status;
+
+// One thread waits (bounded) on an mbarrier that expects an arrival nobody makes.
+__global__ void wait_timeout_selftest_kernel(unsigned int* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    pkv::mbar_init(&bar, 1);
+    pkv::fence_mbar_init();
+    if (!pkv::mbar_wait_bounded(&bar, 0u)) atomicOr(status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
+}
 
 std::atomic<uint64_t> g_launches{0};
 std::mutex g_status_mu;
@@ -307,5 +317,14 @@ int pkv_get_device_status(void* stream, uint32_t* flags) {
 }
 
 uint64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pkv_selftest_wait_timeout(void* stream) {
+    unsigned int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return PKV_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PKV_OK;
+}
 
 }  // extern "C"

@@ -80,6 +80,7 @@ def lib():
         "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
+        "pkv_selftest_wait_timeout": (ctypes.c_int, [vp]),
         "pkv_mgr_create": (vp, [c_i32, c_i32, i32p]),
         "pkv_mgr_clone": (vp, [vp]),
         "pkv_mgr_destroy": (None, [vp]),
@@ -276,6 +277,11 @@ def pkv_paged_prefill_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, 
         _dev(query_start, "query_start", t.int32, (n_seqs + 1,)), n_seqs, n_tokens, int(max_query_len),
         float(scale), _dev(out, "out", dt, qshape), _stream_handle(stream))
     _check(rc, "pkv_paged_prefill_attention")
+
+
+def pkv_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nobody completes; it gives up and flags the status)."""
+    _check(lib().pkv_selftest_wait_timeout(_stream_handle(stream)), "pkv_selftest_wait_timeout")
 
 
 def pkv_copy_blocks(desc: CacheDesc, k_pool, v_pool, pairs, stream=None) -> None:

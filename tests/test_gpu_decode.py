@@ -243,3 +243,19 @@ def test_large_batch(dtype, n_q, n_kv, d):
     lens = rng.integers(0, 90, size=1100)
     lens[:8] = (1, 16, 17, 300, 700, 1100, 0, 64)
     check(dtype, lens, n_q, n_kv, d, seed=61)
+
+
+def test_bounded_wait_gives_up_and_context_stays_usable():
+    """Failure detection without a fault: a wait on an mbarrier nothing completes gives up after its
+    limit, the kernel records PKV_DEV_WAIT_TIMEOUT and returns; the context then runs a normal
+    decode that matches the oracle."""
+    import time
+    assert pkv.pkv_get_device_status() == 0
+    t0 = time.perf_counter()
+    pkv.pkv_selftest_wait_timeout()
+    flags = pkv.pkv_get_device_status()
+    waited = time.perf_counter() - t0
+    assert flags == pkv.PKV_DEV_WAIT_TIMEOUT
+    assert 0.5 < waited < 10.0
+    assert pkv.pkv_get_device_status() == 0          # reading cleared it
+    check("f16", [5, 40, 300], 4, 2, 64, seed=31)     # the context is still healthy
