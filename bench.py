@@ -163,7 +163,7 @@ def build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0, lay
 
 
 def _build_workload(name: str, warmup: int, steps: int, seed_offset: int = 0):
-    extra = warmup + 2 * steps + 2 * W.BLOCK
+    extra = warmup + 3 * steps + 2 * W.BLOCK  # warm-up, the value pass, the roofline pass, e2e
     if name == "gpt":
         wl = W.gpt(seed=W.BASE_SEED + 1 + seed_offset, extra_tokens_per_seq=extra)
         desc = "gpt: 32 layers x 32 heads x head_dim 128 fp16 (512 KiB/token), batch 64, block 16, " \
@@ -201,7 +201,7 @@ def setup_gpu_case(name: str, warmup: int, steps: int, device, seed_offset: int 
     order = W.free_order(wl.num_blocks, wl.seed) if placement == "shuffled" else None
     cache = PagedKVCache(desc, free_order=order, device=device, init="randn",
                          seed=wl.seed)
-    extra = warmup + 2 * steps + 2 * W.BLOCK
+    extra = warmup + 3 * steps + 2 * W.BLOCK  # warm-up, the value pass, the roofline pass, e2e
     if churn is None:
         for s, n in enumerate(wl.context_lens):
             cache.add_sequence(s, int(n) - 1)   # the first step appends the token that makes ctx
@@ -276,6 +276,8 @@ def run_gpu(args) -> dict | None:
     cursor = {"i": 0}
 
     def on_decode(layer, when):
+        if when == "pre":
+            return
         e = ev_pairs[cursor["i"]]
         if when == "start":
             e[0].record(stream)
@@ -294,21 +296,26 @@ def run_gpu(args) -> dict | None:
     kv_bytes = 0
     cow_pairs = 0
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(args.steps):  # value: the steps alone (a timing event per launch would add a gap)
+        st = batch.plan()
+        batch.upload(st)
+        batch.run_device(st, q, k_new, v_new, out, scale)
+        kv_bytes += batch.kv_bytes_last_step()
+        cow_pairs += st["npairs"]
+        apply_churn(cache, batch, state)
+    t1.record(stream)
+    for _ in range(args.steps):  # roofline: the same steps again, each decode launch between two events
         st = batch.plan()
         batch.upload(st)
         batch.run_device(st, q, k_new, v_new, out, scale, on_decode)
         b = batch.kv_bytes_last_step()
-        kv_bytes += b
         layer_bytes.extend([b // L] * L)
-        cow_pairs += st["npairs"]
         apply_churn(cache, batch, state)
-    t1.record(stream)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    launches = pkv.pkv_launch_count() - launches0
+    launches = (pkv.pkv_launch_count() - launches0) // 2  # per pass
     elapsed_ms = t0.elapsed_time(t1)
     elapsed_ms = reduce_over_ranks(elapsed_ms, "max", device)
     total_bytes = reduce_over_ranks(kv_bytes, "sum", device)
@@ -439,15 +446,22 @@ def run_prefill_gpu(args) -> dict | None:
     scale = 1.0 / float(np.sqrt(d))
     seq = 1
 
-    def one_step(on_attn=None, bufs=None):
+    def one_step(on_attn=None, host=None):
         nonlocal seq
         flops = 0.0
         for i, (c0, n) in enumerate(chunks):
-            if bufs is not None:
-                bufs(c0, n)
+            hook = on_attn
+            if host is not None:  # per-layer copies of this chunk's rows, overlapped with the kernels
+                pipe, hq, hk, hv, hout = host
+                pipe.upload_all([[(q[l, c0:c0 + n], hq[l, c0:c0 + n]), (k_new[l, c0:c0 + n], hk[l, c0:c0 + n]),
+                                  (v_new[l, c0:c0 + n], hv[l, c0:c0 + n])] for l in range(L)],
+                                [[(hout[l, c0:c0 + n], out[l, c0:c0 + n])] for l in range(L)])
+                hook = pipe.hook
             st = ps.step([(seq, n, i == 0)], q[:, c0:c0 + n], k_new[:, c0:c0 + n], v_new[:, c0:c0 + n],
-                         out[:, c0:c0 + n], scale, on_attn)
+                         out[:, c0:c0 + n], scale, hook)
             flops += PrefillStep.attention_flops(st, n_q, d) * L
+        if host is not None:
+            host[0].finish()  # the prompt's outputs are on the host
         cache.free(seq)       # host only: the next step admits the prompt again
         seq += 1
         return flops
@@ -462,6 +476,8 @@ def run_prefill_gpu(args) -> dict | None:
     cur = {"i": 0}
 
     def on_attn(layer, when):
+        if when == "pre":
+            return
         e = ev[cur["i"]]
         if when == "start":
             e[0].record(stream)
@@ -478,14 +494,16 @@ def run_prefill_gpu(args) -> dict | None:
     launches0 = pkv.pkv_launch_count()
     flops = 0.0
     t0.record(stream)
-    for _ in range(args.steps):
-        flops += one_step(on_attn)
+    for _ in range(args.steps):  # value: the steps alone
+        flops += one_step()
     t1.record(stream)
+    for _ in range(args.steps):  # roofline: the same steps, each prefill launch between two events
+        one_step(on_attn)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    launches = pkv.pkv_launch_count() - launches0
+    launches = (pkv.pkv_launch_count() - launches0) // 2  # per pass
     if pkv.pkv_get_device_status(stream):
         raise RuntimeError("device status flags set during the timed region")
     ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
@@ -493,25 +511,19 @@ def run_prefill_gpu(args) -> dict | None:
     attn_ms = sum(a.elapsed_time(b) for a, b in ev)
     achieved = flops / (attn_ms * 1e-3) / 1e12
 
-    # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory, outputs back
+    # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory, outputs back,
+    # per layer on copy streams overlapped with the kernels (engine.LayerCopyPipeline)
+    from paged_kv_cache_258_gb300.engine import LayerCopyPipeline
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k_new, v_new))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-
-    def bufs(c0, n):
-        with torch.cuda.stream(stream):
-            q[:, c0:c0 + n].copy_(hq[:, c0:c0 + n], non_blocking=True)
-            k_new[:, c0:c0 + n].copy_(hk[:, c0:c0 + n], non_blocking=True)
-            v_new[:, c0:c0 + n].copy_(hv[:, c0:c0 + n], non_blocking=True)
-
+    host = (LayerCopyPipeline(L, stream, device), hq, hk, hv, hout)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     e2e_flops = 0.0
     for _ in range(args.steps):
-        e2e_flops += one_step(bufs=bufs)
-        with torch.cuda.stream(stream):
-            hout.copy_(out, non_blocking=True)
+        e2e_flops += one_step(host=host)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", device)
@@ -599,14 +611,16 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
     t1 = torch.cuda.Event(enable_timing=True)
     kv = 0
     npairs = 0
+    from paged_kv_cache_258_gb300.engine import LayerCopyPipeline
+    pipe = LayerCopyPipeline(q.shape[0], stream, device)
+    ups = [[(q[l], hq[l]), (k_new[l], hk[l]), (v_new[l], hv[l])] for l in range(q.shape[0])]
+    downs = [[(hout[l], out[l])] for l in range(q.shape[0])]
     t0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
-            q.copy_(hq, non_blocking=True)
-            k_new.copy_(hk, non_blocking=True)
-            v_new.copy_(hv, non_blocking=True)
-            st = batch.step(q, k_new, v_new, out, scale)
-            hout.copy_(out, non_blocking=True)
+            pipe.upload_all(ups, downs)  # layer l's rows go up while earlier layers compute
+            st = batch.step(q, k_new, v_new, out, scale, on_decode=pipe.hook)
+            pipe.finish()                # the step's outputs are on the host
             kv += batch.kv_bytes_last_step()
             npairs += st["npairs"]
             apply_churn(cache, batch, state)
@@ -803,7 +817,7 @@ def run_serve_gpu(args) -> dict | None:
                 time.sleep(dt_)
 
         def on_kernel(kind, layer, when):
-            if not timed_events or kind != "decode":
+            if not timed_events or kind != "decode" or when == "pre":
                 return
             if when == "start":
                 evs.append([torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)])
