@@ -8,8 +8,8 @@ method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAtten
   1. host:   the block manager reserves one slot per sequence (taking a fresh block or
              copying a shared tail on write) and packs the block tables;
   2. H2D:    slots, tables, lengths and copy pairs go to the device in one copy (one pinned
-             image per step, double-buffered so the host can plan step i+1 while step i's copy is
-             pending);
+             image per step, double-buffered on the host and on the device, on an upload stream:
+             step i+1's copy overlaps step i's kernels);
   3. device: copy-on-write block copies, then per layer the KV append and the paged decode
              attention -- copies before appends (else a copy would overwrite the new row),
              appends before attention (the new token attends to itself). By default the append
@@ -86,9 +86,17 @@ class DecodeBatch:
         self._o_len = self._o_tab + n * mb
         self._o_pair = self._o_len + n
         self._meta_words = self._o_pair + 2 * max(n, 1)
-        d_meta = torch.empty(self._meta_words, dtype=torch.int32, device=dev)
-        self.d_meta = d_meta
-        self.d_slots, self.d_tables, self.d_lens, self.d_pairs = self._views(d_meta)
+        # two device copies of the image, filled on an upload stream: step i+1's metadata goes up
+        # while step i's kernels run; a copy is refilled only after the kernels that read it are done
+        self.up_stream = torch.cuda.Stream(dev)
+        self._dev = []
+        for _ in range(2):
+            d_meta = torch.empty(self._meta_words, dtype=torch.int32, device=dev)
+            slots, tables, lens, pairs = self._views(d_meta)
+            self._dev.append(dict(meta=d_meta, slots=slots, tables=tables, lens=lens, pairs=pairs,
+                                  uploaded=torch.cuda.Event(), read=torch.cuda.Event(), used=False))
+        self.d_slots, self.d_tables, self.d_lens, self.d_pairs = (self._dev[0][k] for k in ("slots", "tables", "lens",
+                                                                                             "pairs"))
         self.workspace = pkv.alloc_workspace(cache.desc, n, mb, device=dev)
         # two pinned staging images
         self._stage = []
@@ -128,6 +136,7 @@ class DecodeBatch:
     def plan(self) -> dict:
         """Host part of a step: reserve slots, collect CoW pairs, pack tables (pinned)."""
         st = self._stage[self._turn]
+        st["buf"] = self._turn
         self._turn ^= 1
         if st["used"]:
             st["done"].synchronize()  # the GPU has consumed this staging set
@@ -154,15 +163,22 @@ class DecodeBatch:
     def upload(self, st: dict) -> None:
         import torch
         words = self._o_pair + 2 * st["npairs"]  # only the pairs this step emitted
-        with torch.cuda.stream(self.stream):
-            self.d_meta[:words].copy_(st["meta"][:words], non_blocking=True)
-            st["done"].record(self.stream)
+        dv = self._dev[st["buf"]]
+        with torch.cuda.stream(self.up_stream):
+            if dv["used"]:
+                self.up_stream.wait_event(dv["read"])  # the kernels of two steps ago are done with it
+            dv["meta"][:words].copy_(st["meta"][:words], non_blocking=True)
+            dv["uploaded"].record(self.up_stream)
+            st["done"].record(self.up_stream)
         st["used"] = True
 
     def run_device(self, st: dict, q, k_new, v_new, out, scale: float, on_decode=None) -> None:
         """q/out [L, n, n_q, d]; k_new/v_new [L, n, n_kv, d] device tensors."""
         c = self.cache
         d = c.desc
+        dv = self._dev[st["buf"]]
+        self.stream.wait_event(dv["uploaded"])
+        self.d_slots, self.d_tables, self.d_lens, self.d_pairs = dv["slots"], dv["tables"], dv["lens"], dv["pairs"]
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self.d_pairs[: st["npairs"]], stream=self.stream)
         for layer in range(d.n_layers):
@@ -183,6 +199,8 @@ class DecodeBatch:
                                                scale, out[layer], self.workspace, stream=self.stream)
             if on_decode is not None:
                 on_decode(layer, "end")
+        dv["read"].record(self.stream)
+        dv["used"] = True
 
     def step(self, q, k_new, v_new, out, scale: float, on_decode=None) -> dict:
         st = self.plan()
