@@ -71,7 +71,7 @@ def check(dtype, lens, n_new, n_q, n_kv, d, seed, **kw):
 
 
 # whole prompts, chunks ending mid-block, single tokens, an empty chunk, chunks spanning several
-# query tiles (128 rows per CTA) and several 64-key tiles with ragged tails
+# query tiles (128 rows per CTA) and several 128-key tiles with ragged tails
 LENS = [300, 77, 1, 16, 17, 640, 129, 33]
 NEW = [300, 45, 1, 0, 17, 200, 64, 1]
 
@@ -201,3 +201,26 @@ def test_host_argument_errors():
     out = q.clone()
     pkv.pkv_paged_prefill_attention(desc, 0, q, pool, pool, t, ln, qs, 0, 1.0, out)   # no-op
     assert pkv.pkv_get_device_status() == 0
+
+
+@pytest.mark.parametrize("trial", range(12))
+def test_random_batches_stress(trial):
+    """Random mixes of sequences, chunk lengths, contexts and GQA groups (head_dim 256 runs in
+    clusters of four CTAs sharing K/V loads; its edges -- query tiles with no rows, tiles only
+    some CTAs of a cluster need -- appear throughout). Every output against the oracle; the
+    status word must stay clean (no bounded wait may give up)."""
+    rng = np.random.default_rng(1000 + trial)
+    dtype = ["bf16", "f16"][trial % 2]
+    d = [256, 256, 128, 64][trial % 4]
+    group = int(rng.choice([1, 2, 4, 8]))
+    n_kv = int(rng.integers(1, 3))
+    n_seqs = int(rng.integers(1, 5))
+    lens, new = [], []
+    for _ in range(n_seqs):
+        c = int(rng.integers(1, 1200))
+        n = int(rng.integers(0, min(c, 700) + 1))
+        lens.append(c)
+        new.append(n)
+    if sum(new) == 0:
+        new[0] = lens[0]
+    check(dtype, lens, new, group * n_kv, n_kv, d, seed=2000 + trial)
