@@ -9,8 +9,9 @@
 // 0 .. p. Unlike decode this is a dense contraction (n query rows x c keys x head_dim).
 //
 // CTA = (128 query rows, KV head, sequence); rows = token x head-in-group (GQA rows packed, so each
-// K/V tile serves all G heads). Tiles are BN = 128 keys (eight 16-token blocks): a tcgen05.mma costs
-// about the same at N = 64 as at N = 128, so S = Q K^T runs as N = 128 instructions. Seven warps:
+// K/V tile serves all G heads). Tiles are BN = 128 keys (eight 16-token blocks), so S = Q K^T runs as
+// N = 128 instructions: ~64 cycles each on the tensor pipe, against ~50 cycles for one thread to
+// issue one (an N = 64 instruction would leave the pipe waiting for its issuer). Eight warps:
 //   warps 0-3  softmax: thread t owns query row t, which is TMEM lane t (a warp reaches only its
 //              own 32 lanes). It first writes its row of Q into TMEM (the A operand of S = Q K^T:
 //              no shared-memory reads of Q per instruction), then per tile reads its row of S,
@@ -21,9 +22,11 @@
 //              into rings of STK / STV stages with TMA tensor copies (128-byte swizzle); a K stage
 //              is released when S_j is done, a V stage when PV_j is; warp 6 zeroes the V rows of
 //              skipped blocks and of the positions past the context;
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of SB TMEM buffers (128 x BN fp32),
-//              then O += P_j V_j into a TMEM accumulator (128 x D fp32, one N = D instruction per
-//              16 keys), each followed by a tcgen05.commit onto an mbarrier.
+//   warp 5     S issuer (one thread): S_j = Q K_j^T into one of SB TMEM buffers (128 x BN fp32),
+//              then a tcgen05.commit onto an mbarrier;
+//   warp 7     PV issuer (one thread): O += P_j V_j into a TMEM accumulator (128 x D fp32, one
+//              N = D instruction per 16 keys), then a commit. Two issuers keep the pipe fed while
+//              each waits on its own barriers.
 // S_{j+1} runs on the tensor pipe while the softmax warps work on S_j (they read S_j into registers
 // first and release its buffer).
 // O is rescaled (read, multiplied, written back in TMEM) only when a row's running maximum grows
@@ -76,8 +79,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 template <int D>
 struct UmmaTuning {
-    // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (a tcgen05.mma costs about
-    // the same time at N = 64 as at N = 128 on this part: small N wastes the tensor pipe).
+    // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (one issuing thread cannot
+    // keep up with N = 64 instructions).
     static constexpr int BN = 128;
     // CTAs per cluster sharing K/V loads: at head_dim 256 every CTA would pull 128 KiB per 128-key
     // tile from L2 (the measured limit), so the four CTAs of a cluster, which hold adjacent query
@@ -116,7 +119,7 @@ struct UmmaSmem {
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(256, 1)
     paged_prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v) {
     static_assert(128 % G == 0, "whole tokens per tile");
@@ -236,15 +239,19 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t ring = (uint32_t)(is_v ? S::V : S::K);
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
         int issued = 0;
+        // lane l < BPT handles block l of every tile; its table entry is read one tile ahead, so
+        // that the load's latency overlaps the wait for a free stage
+        int phys_next = lane < BPT && lane < nb ? __ldg(trow + lane) : -1;
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j % nst;
+            const int blk = j * BPT + lane;
+            const bool inb = lane < BPT && blk < nb;
+            const int phys = phys_next;
+            phys_next = lane < BPT && blk + BPT < nb ? __ldg(trow + blk + BPT) : -1;
             if (j >= nst && !mbar_wait_bounded(&empty[st], (uint32_t)((j / nst) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                 break;
             }
-            const int blk = j * BPT + lane;
-            const bool inb = lane < BPT && blk < nb;
-            const int phys = inb ? trow[blk] : -1;
             const bool ok = inb && (unsigned)phys < (unsigned)a.num_blocks;
             const unsigned okm = __ballot_sync(0xffffffffu, ok);
             const unsigned badm = __ballot_sync(0xffffffffu, inb && !ok);
@@ -301,8 +308,13 @@ __global__ void __launch_bounds__(224, 1)
         }
         for (int j = max(0, issued - nst); j < issued; ++j)  // the copies of the last stages have landed
             mbar_wait_bounded(&full[j % nst], (uint32_t)(j / nst) & 1u);
-    } else if (warp == 5) {
-        // ===================== MMA issuer =====================
+    } else if (warp == 5 || warp == 7) {
+        // ===================== MMA issuers: warp 5 S = Q K^T, warp 7 O += P V =====================
+        // Two issuing threads: a tcgen05.mma takes ~50 cycles to issue from one thread and an
+        // N = 128 instruction ~64 cycles on the tensor pipe, so one thread interleaving both products
+        // and their barrier waits would leave the pipe idle. Descriptors are built once per stage
+        // and stepped by constant offsets (shared-memory addresses stay below 2^18 bytes, so the
+        // 14-bit address field never carries).
         if (lane == 0) {
             bool ok = true;
             // a stage of a common tile is released in every CTA of the cluster; a stage only this
@@ -315,68 +327,74 @@ __global__ void __launch_bounds__(224, 1)
                     for (int c = 0; c < CL; ++c) umma_commit(bar);
                 }
             };
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % STK;
-                const int b = j % SB;
-                if (!mbar_wait_bounded(&full_k[st], (uint32_t)(j / STK) & 1u)) return false;
-                if (j >= SB && !mbar_wait_bounded(&s_free[b], (uint32_t)((j / SB) - 1) & 1u)) return false;
-                tcgen05_after_sync();
-                const uint32_t sK = sbase + (uint32_t)S::K + (uint32_t)st * KT;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t bd = umma_desc_sw128(sK + (uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32, 16, 1024);
-                    umma_f16_tmem_a(tmem + S_COL + (uint32_t)(b * BN), tmem + Q_COL + (uint32_t)ks * 8, bd, IDESC_S, ks > 0);
-                }
-                umma_commit(&s_full[b]);
-                release(k_empty + st, j);  // the K stage may take tile j + STK once S_j is done
-                return true;
-            };
-            ok = mbar_wait_bounded(q_ready, 0u) && issue_s(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                const int pb = j % NP;
-                const int sv = j % STV;
-                if (!mbar_wait_bounded(&p_full[pb], (uint32_t)(j / NP) & 1u) ||
-                    !mbar_wait_bounded(&full_v[sv], (uint32_t)(j / STV) & 1u) ||
-                    (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u))) {
-                    ok = false;
-                    break;
-                }
-                tcgen05_after_sync();
-                const uint32_t sP = sbase + (uint32_t)S::P + (uint32_t)pb * (uint32_t)S::PB;
-                const uint32_t sV = sbase + (uint32_t)S::V + (uint32_t)sv * KT;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = umma_desc_sw128(sV + (uint32_t)kk * 2048, PANEL, 1024);
-                    if constexpr (Tu::PT) {
-                        umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd, IDESC_PV,
-                                        j > 0 || kk > 0);
-                    } else {
-                        const uint64_t ad =
-                            umma_desc_sw128(sP + (uint32_t)(kk >> 2) * (128 * 128) + (uint32_t)(kk & 3) * 32, 16, 1024);
-                        umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+            if (warp == 5) {
+                const uint64_t kdesc0 = umma_desc_sw128(sbase + (uint32_t)S::K, 16, 1024);
+                ok = mbar_wait_bounded(q_ready, 0u);
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int st = j % STK;
+                    const int b = j % SB;
+                    if (!mbar_wait_bounded(&full_k[st], (uint32_t)(j / STK) & 1u) ||
+                        (j >= SB && !mbar_wait_bounded(&s_free[b], (uint32_t)((j / SB) - 1) & 1u))) {
+                        ok = false;
+                        break;
                     }
+                    tcgen05_after_sync();
+                    const uint64_t kd = kdesc0 + (uint64_t)(((uint32_t)st * KT) >> 4);
+                    const uint32_t d_s = tmem + S_COL + (uint32_t)(b * BN);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_f16_tmem_a(d_s, tmem + Q_COL + (uint32_t)ks * 8,
+                                        kd + (uint64_t)(((uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32) >> 4),
+                                        IDESC_S, ks > 0);
+                    umma_commit(&s_full[b]);
+                    release(k_empty + st, j);  // the K stage may take tile j + STK once S_j is done
                 }
-                umma_commit(&p_free[pb]);
-                release(v_empty + sv, j);
+            } else {
+                const uint64_t vdesc0 = umma_desc_sw128(sbase + (uint32_t)S::V, PANEL, 1024);
+                const uint64_t pdesc0 = umma_desc_sw128(sbase + (uint32_t)S::P, 16, 1024);
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int pb = j % NP;
+                    const int sv = j % STV;
+                    if (!mbar_wait_bounded(&p_full[pb], (uint32_t)(j / NP) & 1u) ||
+                        !mbar_wait_bounded(&full_v[sv], (uint32_t)(j / STV) & 1u) ||
+                        (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u))) {
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_after_sync();
+                    const uint64_t vd = vdesc0 + (uint64_t)(((uint32_t)sv * KT) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t bd = vd + (uint64_t)(((uint32_t)kk * 2048) >> 4);
+                        if constexpr (Tu::PT) {
+                            umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd,
+                                            IDESC_PV, j > 0 || kk > 0);
+                        } else {
+                            const uint64_t ad = pdesc0 + (uint64_t)(((uint32_t)pb * (uint32_t)S::PB +
+                                                                     (uint32_t)(kk >> 2) * (128 * 128) +
+                                                                     (uint32_t)(kk & 3) * 32) >> 4);
+                            umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                        }
+                    }
+                    umma_commit(&p_free[pb]);
+                    release(v_empty + sv, j);
+                }
             }
             if (!ok) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
-            // every issued MMA has completed before TMEM is released (the last commit covers them all)
             const int last = n_tiles - 1;
-            mbar_wait_bounded(&p_free[last % NP], (uint32_t)(last / NP) & 1u);
+            // this thread's MMAs have completed before TMEM is released (its last commit covers them all)
+            if (warp == 5)
+                mbar_wait_bounded(&s_full[last % SB], (uint32_t)(last / SB) & 1u);
+            else
+                mbar_wait_bounded(&p_free[last % NP], (uint32_t)(last / NP) & 1u);
             if constexpr (CL > 1) {
-                // and every release the other CTA sends here has landed: the last phase of each stage
+                // and every release the other CTAs send here has landed: the last phase of each stage
                 // completes only with all of its arrivals
-                for (int st = 0; st < STK && st < n_tiles; ++st) {
-                    const int jl = st + ((n_tiles - 1 - st) / STK) * STK;
-                    mbar_wait_bounded(&k_empty[st], (uint32_t)(jl / STK) & 1u);
-                }
-                for (int st = 0; st < STV && st < n_tiles; ++st) {
-                    const int jl = st + ((n_tiles - 1 - st) / STV) * STV;
-                    mbar_wait_bounded(&v_empty[st], (uint32_t)(jl / STV) & 1u);
+                const int nst = warp == 5 ? STK : STV;
+                uint64_t* empty = warp == 5 ? k_empty : v_empty;
+                for (int st = 0; st < nst && st < n_tiles; ++st) {
+                    const int jl = st + ((n_tiles - 1 - st) / nst) * nst;
+                    mbar_wait_bounded(&empty[st], (uint32_t)(jl / nst) & 1u);
                 }
             }
         }
@@ -585,7 +603,7 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
     b.q_tiles = (a.q_tiles + CL - 1) / CL * CL;  // whole clusters; the extra query tiles have no rows
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(b.q_tiles, b.n_kv, b.n_seqs);
-    cfg.blockDim = dim3(224, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
