@@ -8,8 +8,8 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const DecodeArgs& a, cud
     const long long rows = (long long)a.num_blocks * a.n_kv * kBlock;
     if (decode_uses_mma(PKV_BF16, group, rows)) {
         CUtensorMap tk, tv;
-        cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, &tk);
-        if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, &tv);
+        cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, PKV_BOX_PANEL, &tk);
+        if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, PKV_BOX_PANEL, &tv);
         if (err != cudaSuccess) return err;
         return launch_decode_mma_dtype<__nv_bfloat16>(head_dim, group, a, tk, tv, stream, n_launches);
     }

@@ -122,7 +122,8 @@ inline bool decode_uses_mma(int dtype, int group, long long rows) {
 }
 
 // Cached TMA tensor map of one pool layer seen as rows x head_dim 16-bit elements (tmap.cu).
-cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, CUtensorMap* out);
+enum { PKV_BOX_PANEL = 0, PKV_BOX_BLOCK = 1 };
+cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, int box, CUtensorMap* out);
 
 // Shared with decode_static.cu (abi.cu owns both): the current device's status word, and the
 // process-wide count of kernels launched by this library.

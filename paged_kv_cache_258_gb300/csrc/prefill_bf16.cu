@@ -7,8 +7,8 @@ cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, c
     const long long rows = (long long)a.num_blocks * a.n_kv * kBlock;
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are 32-bit
     CUtensorMap tk, tv;
-    cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, &tk);
-    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, &tv);
+    cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, PKV_BOX_PANEL, &tk);
+    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, PKV_BOX_BLOCK, &tv);
     if (err != cudaSuccess) return err;
     return launch_prefill_umma_dtype<__nv_bfloat16>(head_dim, group, a, tk, tv, stream);
 }

@@ -7,8 +7,8 @@ cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cu
     const long long rows = (long long)a.num_blocks * a.n_kv * kBlock;
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are 32-bit
     CUtensorMap tk, tv;
-    cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_F16, &tk);
-    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_F16, &tv);
+    cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_F16, PKV_BOX_PANEL, &tk);
+    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_F16, PKV_BOX_BLOCK, &tv);
     if (err != cudaSuccess) return err;
     return launch_prefill_umma_dtype<__half>(head_dim, group, a, tk, tv, stream);
 }

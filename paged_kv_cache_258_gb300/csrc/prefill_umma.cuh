@@ -18,15 +18,19 @@
 //              masks by selection, keeps the running max and sum in registers and writes its row
 //              of P (storage type) into TMEM (d <= 128) or shared memory (d = 256, where TMEM is
 //              full: S 128 + O 256 + Q 128 columns);
-//   warps 4, 6 producers: walk the block table and move the K tiles (warp 4) and V tiles (warp 6)
-//              into rings of STK / STV stages with TMA tensor copies (128-byte swizzle); a K stage
-//              is released when S_j is done, a V stage when PV_j is; warp 6 zeroes the V rows of
-//              skipped blocks and of the positions past the context;
+//   warps 4, 6 producers: walk the block table and move the K tiles (warp 4; a 2-D copy per block
+//              and 64-column panel, landing panel-major so that S = Q K^T reads 128 keys per
+//              instruction) and V stages of VB blocks (warp 6; one 3-D copy per block, landing
+//              block-major: a PV instruction reads one 16-key block) into rings of STK / STV
+//              stages (128-byte swizzle); a K stage is released when S_j is done, a V stage when
+//              the PV instructions that read it are; warp 6 zeroes the V rows of skipped blocks
+//              and of the positions past the context;
 //   warp 5     S issuer (one thread): S_j = Q K_j^T into one of SB TMEM buffers (128 x BN fp32),
 //              then a tcgen05.commit onto an mbarrier;
 //   warp 7     PV issuer (one thread): O += P_j V_j into a TMEM accumulator (128 x D fp32, one
-//              N = D instruction per 16 keys), then a commit. Two issuers keep the pipe fed while
-//              each waits on its own barriers.
+//              N = D instruction per 16 keys), V stage by V stage, each followed by commits that
+//              free that part of P and that V stage. Two issuers keep the pipe fed while each
+//              waits on its own barriers.
 // S_{j+1} runs on the tensor pipe while the softmax warps work on S_j (they read S_j into registers
 // first and release its buffer).
 // O is rescaled (read, multiplied, written back in TMEM) only when a row's running maximum grows
@@ -70,6 +74,25 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* 
         : "memory");
 }
 
+// 3-D tensor copy of one whole (block, KV head) chunk: box 64 columns x 16 rows x D/64 panels,
+// landing as [panel][16 rows][128 B] (tensor map of the PKV_BOX_BLOCK kind).
+__device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const void* tmap, int row, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* tmap, int row, uint64_t* bar,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // 2^x with the ex2.approx.ftz instruction (2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -90,7 +113,11 @@ struct UmmaTuning {
     static constexpr bool PT = D <= 128;          // P in TMEM (A operand of PV) rather than shared memory
     static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
     static constexpr int STK = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K stages
-    static constexpr int STV = D == 256 ? 1 : (D == 128 ? 3 : 4);  // V stages
+    // V stages hold VB 16-key blocks each, block-major ([block][panel][16 rows][128 B], one 3-D TMA
+    // copy per block). At d = 256 shared memory has room for 64 KiB of V next to two K stages and P:
+    // two half-tile stages, so V of tile j+1 streams in while PV_j still reads the other half.
+    static constexpr int VB = D == 256 ? 4 : 8;
+    static constexpr int STV = D == 256 ? 2 : (D == 128 ? 3 : 4);  // V stages
     static constexpr int NP = D == 64 ? 2 : 1;     // P buffers
     // TMEM columns: S [0, SB*BN), O [SB*BN, +D), Q [.., +D/2), P [.., +NP*BN/2) when PT (16-bit
     // operands hold two elements per 32-bit column)
@@ -104,15 +131,18 @@ template <int D>
 struct UmmaSmem {
     using Tu = UmmaTuning<D>;
     static constexpr int BN = Tu::BN;
-    static constexpr size_t KT = (size_t)BN * D * 2;    // K or V tile [D/64][BN keys][128 B]
+    static constexpr size_t KT = (size_t)BN * D * 2;    // K tile [D/64][BN keys][128 B]
+    static constexpr size_t VT = (size_t)Tu::VB * 16 * D * 2;  // V stage [VB][D/64][16 keys][128 B]
     static constexpr size_t PB = Tu::PT ? 0 : (size_t)128 * BN * 2;  // P [BN/64][128 rows][128 B]
     static constexpr size_t K = 0;                       // [STK] K tiles
-    static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V tiles
-    static constexpr size_t P = V + (size_t)Tu::STV * KT;  // [NP] P tiles
+    static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V stages
+    static constexpr size_t P = V + (size_t)Tu::STV * VT;  // [NP] P tiles
     static constexpr size_t BARS = P + (size_t)Tu::NP * PB;
-    // full_k[STK] k_empty[STK] full_v[STV] v_empty[STV] s_full[SB] s_free[SB] p_full[NP] p_free[NP]
+    // full_k[STK] k_empty[STK] full_v[STV] v_empty[STV] s_full[SB] s_free[SB] p_full[NP * VPT]
+    // p_free[NP * VPT] (one pair per part of a P buffer that one V stage's instructions read)
     // vtail q_ready
-    static constexpr int NBARS = 2 * Tu::STK + 2 * Tu::STV + 2 * Tu::SB + 2 * Tu::NP + 2;
+    static constexpr int NPP = Tu::NP * (Tu::BN / 16 / Tu::VB);
+    static constexpr int NBARS = 2 * Tu::STK + 2 * Tu::STV + 2 * Tu::SB + 2 * NPP + 2;
     static constexpr size_t TADDR = BARS + (size_t)NBARS * 8;  // TMEM base address
     static constexpr size_t TOTAL = TADDR + 16;
     static constexpr size_t ALLOC = TOTAL + 1024;
@@ -132,7 +162,13 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int QT = ROWS / G;
     constexpr int PANELS = D / 64;
     constexpr uint32_t KT = (uint32_t)S::KT;
-    constexpr uint32_t PANEL = BN * 128;                // one 64-column panel of a K/V tile
+    constexpr uint32_t VT = (uint32_t)S::VT;
+    constexpr uint32_t PANEL = BN * 128;                // one 64-column panel of a K tile
+    constexpr uint32_t BLKB = kBlock * D * 2;           // one block of one KV head (a V stage holds VB)
+    constexpr int VB = Tu::VB;
+    constexpr int VPT = BPT / VB;                       // V stages per tile
+    static_assert(BPT % VB == 0, "whole V stages per tile");
+    static_assert(Tu::PT ? VPT == 1 : (VB * kBlock) % 64 == 0, "a P part is whole 64-key panels");
     constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t IDESC_S = umma_idesc_f16(BF, 128, BN, false);
     constexpr uint32_t IDESC_PV = umma_idesc_f16(BF, 128, D, true);
@@ -149,8 +185,8 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t* s_full = v_empty + STV;
     uint64_t* s_free = s_full + SB;
     uint64_t* p_full = s_free + SB;
-    uint64_t* p_free = p_full + NP;
-    uint64_t* vtail = p_free + NP;
+    uint64_t* p_free = p_full + S::NPP;
+    uint64_t* vtail = p_free + S::NPP;
     uint64_t* q_ready = vtail + 1;
     uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::TADDR);
     const uint32_t sbase = smem_addr(smem);
@@ -212,7 +248,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 128);
         }
-        for (int i = 0; i < NP; ++i) {
+        for (int i = 0; i < S::NPP; ++i) {
             mbar_init(&p_full[i], 128);
             mbar_init(&p_free[i], 1);
         }
@@ -228,86 +264,101 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t tmem = *taddr_s;
 
     if (warp == 4 || warp == 6) {
-        // ===================== producers: warp 4 moves K tiles, warp 6 moves V tiles =====================
-        // A K stage is released once S_j has been computed, a V stage once O += P_j V_j has: the next
-        // K tile can land while the softmax of this one runs.
+        // ===================== producers: warp 4 moves K tiles, warp 6 moves V stages =====================
+        // A K stage (one tile) is released once S_j has been computed, a V stage (VB blocks) once the
+        // PV instructions that read it have: the next K tile lands while the softmax of this one runs.
+        // Unit u: K tile u (BPT blocks, panel-major, one 2-D copy per block and panel), or V stage u
+        // (VB blocks of tile u / VPT, block-major, one 3-D copy per block).
         const bool is_v = warp == 6;
         const int nst = is_v ? STV : STK;
+        const int upt = is_v ? VPT : 1;           // units per tile
+        const int nbu = is_v ? VB : BPT;          // blocks per unit
+        const int n_units = n_tiles * upt;
         uint64_t* full = is_v ? full_v : full_k;
         uint64_t* empty = is_v ? v_empty : k_empty;
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         const uint32_t ring = (uint32_t)(is_v ? S::V : S::K);
+        const uint32_t ust = is_v ? VT : KT;      // bytes per stage
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
         int issued = 0;
-        // lane l < BPT handles block l of every tile; its table entry is read one tile ahead, so
+        // lane l < nbu handles block l of every unit; its table entry is read one unit ahead, so
         // that the load's latency overlaps the wait for a free stage
-        int phys_next = lane < BPT && lane < nb ? __ldg(trow + lane) : -1;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % nst;
-            const int blk = j * BPT + lane;
-            const bool inb = lane < BPT && blk < nb;
+        int phys_next = lane < nbu && lane < nb ? __ldg(trow + lane) : -1;
+        for (int u = 0; u < n_units; ++u) {
+            const int j = u / upt;
+            const int st = u % nst;
+            const int blk = u * nbu + lane;      // units tile the block list in order
+            const bool inb = lane < nbu && blk < nb;
             const int phys = phys_next;
-            phys_next = lane < BPT && blk + BPT < nb ? __ldg(trow + blk + BPT) : -1;
-            if (j >= nst && !mbar_wait_bounded(&empty[st], (uint32_t)((j / nst) - 1) & 1u)) {
+            phys_next = lane < nbu && blk + nbu < nb ? __ldg(trow + blk + nbu) : -1;
+            if (u >= nst && !mbar_wait_bounded(&empty[st], (uint32_t)((u / nst) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                 break;
             }
             const bool ok = inb && (unsigned)phys < (unsigned)a.num_blocks;
             const unsigned okm = __ballot_sync(0xffffffffu, ok);
             const unsigned badm = __ballot_sync(0xffffffffu, inb && !ok);
-            unsigned char* tile_ptr = smem + ring + (size_t)st * KT;
+            unsigned char* unit_ptr = smem + ring + (size_t)st * ust;
             if (badm) {
                 // skipped blocks: keys masked by the softmax, V rows zeroed (P = 0 there, 0 * NaN is not)
                 if (!is_v && lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_BAD_BLOCK_ID);
                 if (is_v) {
-                    for (int b = 0; b < BPT; ++b) {
+                    for (int b = 0; b < VB; ++b) {
                         if (!((badm >> b) & 1u)) continue;
-                        for (int i = lane; i < PANELS * 128; i += 32) {  // 2 KiB per panel = 128 x 16 B
-                            const int pn = i / 128;
-                            reinterpret_cast<uint4*>(tile_ptr + (size_t)pn * PANEL + (size_t)b * 2048)[i % 128] =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
+                        for (int i = lane; i < (int)(BLKB / 16); i += 32)
+                            reinterpret_cast<uint4*>(unit_ptr + (size_t)b * BLKB)[i] = make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
             }
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(okm) * (uint32_t)(kBlock * D * 2));
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(okm) * BLKB);
             __syncwarp();
             if (ok) {
                 const int row0 = (phys * a.n_kv + g) * kBlock;
-                const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
-                if (CL > 1 && j < n_common) {
-                    // common tile: this CTA loads its share of the blocks into every CTA of the cluster
-                    if ((uint32_t)lane * CL / BPT == crank) {
+                // common tile: this CTA loads its share of the blocks into every CTA of the cluster
+                const bool mc = CL > 1 && j < n_common;
+                if (!mc || (uint32_t)lane * CL / (uint32_t)nbu == crank) {
+                    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
+                    if (is_v) {
+                        const uint32_t dst = sbase + ring + (uint32_t)st * VT + (uint32_t)lane * BLKB;
+                        if (mc)
+                            tma_load_3d_multicast(dst, tm, row0, &full[st], mask);
+                        else
+                            tma_load_3d_keep(dst, tm, row0, &full[st]);
+                    } else {
+                        const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
 #pragma unroll
-                        for (int pn = 0; pn < PANELS; ++pn)
-                            tma_load_2d_multicast(dst + pn * PANEL, tm, pn * 64, row0, &full[st], (uint16_t)((1u << CL) - 1u));
+                        for (int pn = 0; pn < PANELS; ++pn) {
+                            if (mc)
+                                tma_load_2d_multicast(dst + pn * PANEL, tm, pn * 64, row0, &full[st], mask);
+                            else
+                                tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
+                        }
                     }
-                } else {
-#pragma unroll
-                    for (int pn = 0; pn < PANELS; ++pn) tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
                 }
             }
-            issued = j + 1;
+            issued = u + 1;
             if (is_v && j == n_tiles - 1 && tail_tile) {
-                if (!mbar_wait_bounded(&full_v[st], (uint32_t)(j / nst) & 1u)) {
+                // zero this stage's rows past the context (key rows r0 .. BN-1 of the last tile)
+                if (!mbar_wait_bounded(&full_v[st], (uint32_t)(u / nst) & 1u)) {
                     if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                     break;
                 }
-                const int r0 = ctx - j * BN;  // first key row past the context, 1 .. BN-1
-                for (int i = lane; i < PANELS * (BN - r0) * 8; i += 32) {
-                    const int pn = i / ((BN - r0) * 8);
-                    const int rem = i % ((BN - r0) * 8);
-                    reinterpret_cast<uint4*>(tile_ptr + (size_t)pn * PANEL + (size_t)(r0 + rem / 8) * 128)[rem % 8] =
-                        make_uint4(0u, 0u, 0u, 0u);
+                const int r0 = ctx - j * BN;               // 1 .. BN-1
+                const int lo = max(r0 - (u % VPT) * VB * kBlock, 0);  // first stage row to zero
+                for (int i = lane; i < (VB * kBlock - lo) * PANELS * 8; i += 32) {
+                    const int r = lo + i / (PANELS * 8);   // stage row = 16 x block + token
+                    const int pn = (i / 8) % PANELS;
+                    reinterpret_cast<uint4*>(unit_ptr + (size_t)(r / kBlock) * BLKB + (size_t)pn * 2048 +
+                                             (size_t)(r % kBlock) * 128)[i % 8] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(vtail);
+                if (u == n_units - 1) mbar_arrive(vtail);
             }
         }
-        for (int j = max(0, issued - nst); j < issued; ++j)  // the copies of the last stages have landed
-            mbar_wait_bounded(&full[j % nst], (uint32_t)(j / nst) & 1u);
+        for (int u = max(0, issued - nst); u < issued; ++u)  // the copies of the last stages have landed
+            mbar_wait_bounded(&full[u % nst], (uint32_t)(u / nst) & 1u);
     } else if (warp == 5 || warp == 7) {
         // ===================== MMA issuers: warp 5 S = Q K^T, warp 7 O += P V =====================
         // Two issuing threads: a tcgen05.mma takes ~50 cycles to issue from one thread and an
@@ -350,34 +401,45 @@ __global__ void __launch_bounds__(256, 1)
                     release(k_empty + st, j);  // the K stage may take tile j + STK once S_j is done
                 }
             } else {
-                const uint64_t vdesc0 = umma_desc_sw128(sbase + (uint32_t)S::V, PANEL, 1024);
+                // V stage: block kk of the tile at + (kk % VB) * BLKB, its panels 2 KiB apart (leading
+                // byte offset), 8-key core groups 1 KiB apart (stride byte offset)
+                const uint64_t vdesc0 = umma_desc_sw128(sbase + (uint32_t)S::V, 2048, 1024);
                 const uint64_t pdesc0 = umma_desc_sw128(sbase + (uint32_t)S::P, 16, 1024);
-                for (int j = 0; j < n_tiles; ++j) {
+                for (int j = 0; ok && j < n_tiles; ++j) {
                     const int pb = j % NP;
-                    const int sv = j % STV;
-                    if (!mbar_wait_bounded(&p_full[pb], (uint32_t)(j / NP) & 1u) ||
-                        !mbar_wait_bounded(&full_v[sv], (uint32_t)(j / STV) & 1u) ||
-                        (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u))) {
+                    if (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u)) {
                         ok = false;
                         break;
                     }
-                    tcgen05_after_sync();
-                    const uint64_t vd = vdesc0 + (uint64_t)(((uint32_t)sv * KT) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t bd = vd + (uint64_t)(((uint32_t)kk * 2048) >> 4);
-                        if constexpr (Tu::PT) {
-                            umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd,
-                                            IDESC_PV, j > 0 || kk > 0);
-                        } else {
-                            const uint64_t ad = pdesc0 + (uint64_t)(((uint32_t)pb * (uint32_t)S::PB +
-                                                                     (uint32_t)(kk >> 2) * (128 * 128) +
-                                                                     (uint32_t)(kk & 3) * 32) >> 4);
-                            umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                    for (int h = 0; h < VPT; ++h) {
+                        // part h of P_j (the keys of V stage u) and the V stage itself
+                        const int u = j * VPT + h;
+                        const int sv = u % STV;
+                        if (!mbar_wait_bounded(&p_full[pb * VPT + h], (uint32_t)(j / NP) & 1u) ||
+                            !mbar_wait_bounded(&full_v[sv], (uint32_t)(u / STV) & 1u)) {
+                            ok = false;
+                            break;
                         }
+                        tcgen05_after_sync();
+                        const uint64_t vd = vdesc0 + (uint64_t)(((uint32_t)sv * VT) >> 4);
+#pragma unroll
+                        for (int i = 0; i < VB; ++i) {
+                            const int kk = h * VB + i;
+                            const uint64_t bd = vd + (uint64_t)(((uint32_t)i * BLKB) >> 4);
+                            if constexpr (Tu::PT) {
+                                umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd,
+                                                IDESC_PV, j > 0 || kk > 0);
+                            } else {
+                                const uint64_t ad = pdesc0 + (uint64_t)(((uint32_t)pb * (uint32_t)S::PB +
+                                                                         (uint32_t)(kk >> 2) * (128 * 128) +
+                                                                         (uint32_t)(kk & 3) * 32) >> 4);
+                                umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                            }
+                        }
+                        umma_commit(&p_free[pb * VPT + h]);  // part h of P buffer pb may take P_{j+NP}
+                        release(v_empty + sv, j);            // the V stage may take unit u + STV
                     }
-                    umma_commit(&p_free[pb]);
-                    release(v_empty + sv, j);
                 }
             }
             if (!ok) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
@@ -386,15 +448,16 @@ __global__ void __launch_bounds__(256, 1)
             if (warp == 5)
                 mbar_wait_bounded(&s_full[last % SB], (uint32_t)(last / SB) & 1u);
             else
-                mbar_wait_bounded(&p_free[last % NP], (uint32_t)(last / NP) & 1u);
+                mbar_wait_bounded(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u);
             if constexpr (CL > 1) {
                 // and every release the other CTAs send here has landed: the last phase of each stage
                 // completes only with all of its arrivals
                 const int nst = warp == 5 ? STK : STV;
+                const int n_units = warp == 5 ? n_tiles : n_tiles * VPT;
                 uint64_t* empty = warp == 5 ? k_empty : v_empty;
-                for (int st = 0; st < nst && st < n_tiles; ++st) {
-                    const int jl = st + ((n_tiles - 1 - st) / nst) * nst;
-                    mbar_wait_bounded(&empty[st], (uint32_t)(jl / nst) & 1u);
+                for (int st = 0; st < nst && st < n_units; ++st) {
+                    const int ul = st + ((n_units - 1 - st) / nst) * nst;
+                    mbar_wait_bounded(&empty[st], (uint32_t)(ul / nst) & 1u);
                 }
             }
         }
@@ -486,7 +549,7 @@ __global__ void __launch_bounds__(256, 1)
             const float alpha = grow ? exp2f(m_used - m_new) : 1.f;  // 0 when m_used is -inf
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // O holds P_0..P_{j-1} V: wait for the last PV, then scale this warp's 32 rows in TMEM
-                if (!mbar_wait_bounded(&p_free[(j - 1) % NP], (uint32_t)((j - 1) / NP) & 1u)) {
+                if (!mbar_wait_bounded(&p_free[((j - 1) % NP) * VPT + VPT - 1], (uint32_t)((j - 1) / NP) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -519,36 +582,40 @@ __global__ void __launch_bounds__(256, 1)
                 ls[c & 7] += p0 + p1;
             }
             l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            // P buffer pb is free once PV_{j-NP} has completed
-            if (j >= NP && !mbar_wait_bounded(&p_free[pb], (uint32_t)((j / NP) - 1) & 1u)) {
-                ok = false;
-                break;
+            // part h of P buffer pb is free once the instructions of PV_{j-NP} that read it are done
+#pragma unroll
+            for (int h = 0; h < VPT; ++h) {
+                if (j >= NP && !mbar_wait_bounded(&p_free[pb * VPT + h], (uint32_t)((j / NP) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                if constexpr (Tu::PT) {
+                    // this row of P -> TMEM lane `row`, two 16-bit weights per column
+                    if (j >= NP) tcgen05_after_sync();
+#pragma unroll
+                    for (int c0 = 0; c0 < BN / 2; c0 += 32)
+                        tmem_st32(tmem + lane_base + Tu::P_COL + (uint32_t)(pb * (BN / 2) + c0),
+                                  *reinterpret_cast<const uint32_t(*)[32]>(&pw[c0]));
+                    tmem_wait_st();
+                } else {
+                    unsigned char* prow = smem + S::P + (size_t)pb * S::PB + (size_t)row * 128;
+#pragma unroll
+                    for (int pp = h * (VB * kBlock / 64); pp < (h + 1) * (VB * kBlock / 64); ++pp)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(prow + (size_t)pp * (128 * 128) + ((c ^ (row & 7)) << 4)) =
+                                make_uint4(pw[32 * pp + 4 * c], pw[32 * pp + 4 * c + 1], pw[32 * pp + 4 * c + 2],
+                                           pw[32 * pp + 4 * c + 3]);
+                    fence_proxy_async_smem();
+                }
+                tcgen05_before_sync();
+                mbar_arrive(&p_full[pb * VPT + h]);
             }
-            if constexpr (Tu::PT) {
-                // this row of P -> TMEM lane `row`, two 16-bit weights per column
-                if (j >= NP) tcgen05_after_sync();
-#pragma unroll
-                for (int c0 = 0; c0 < BN / 2; c0 += 32)
-                    tmem_st32(tmem + lane_base + Tu::P_COL + (uint32_t)(pb * (BN / 2) + c0),
-                              *reinterpret_cast<const uint32_t(*)[32]>(&pw[c0]));
-                tmem_wait_st();
-            } else {
-                unsigned char* prow = smem + S::P + (size_t)pb * S::PB + (size_t)row * 128;
-#pragma unroll
-                for (int pp = 0; pp < BN / 64; ++pp)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(prow + (size_t)pp * (128 * 128) + ((c ^ (row & 7)) << 4)) =
-                            make_uint4(pw[32 * pp + 4 * c], pw[32 * pp + 4 * c + 1], pw[32 * pp + 4 * c + 2],
-                                       pw[32 * pp + 4 * c + 3]);
-                fence_proxy_async_smem();
-            }
-            tcgen05_before_sync();
-            mbar_arrive(&p_full[pb]);
+            if (!ok) break;
         }
         if (ok) {
             const int last = n_tiles - 1;
-            if (!mbar_wait_bounded(&p_free[last % NP], (uint32_t)(last / NP) & 1u)) ok = false;
+            if (!mbar_wait_bounded(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u)) ok = false;
         }
         if (!ok) {
             if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);

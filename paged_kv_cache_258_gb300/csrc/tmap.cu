@@ -1,10 +1,16 @@
 // tmap.cu -- TMA tensor maps over one layer of a K or V pool (host side).
 //
-// A pool layer [num_blocks][n_kv][16][D] of 16-bit elements is described as a 2-D tensor of
-// num_blocks*n_kv*16 rows by D columns; the decode kernel copies 64-column x 16-row boxes (one
-// panel of one (block, KV head) chunk) with the 128-byte swizzle. Encoding goes through the driver
-// entry point cuTensorMapEncodeTiled, found once through the runtime; maps are cached by
-// (address, shape, type, device) so steady-state calls do not re-encode.
+// A pool layer [num_blocks][n_kv][16][D] of 16-bit elements is described as a tensor of
+// num_blocks*n_kv*16 rows by D columns, copied with the 128-byte swizzle in one of two box shapes:
+//   PKV_BOX_PANEL  2-D, a 64-column x 16-row box: one 64-column panel of one (block, KV head)
+//                  chunk, placed by the caller (decode, and the K tiles of prefill, whose panels
+//                  of several blocks must sit in one [panel][rows] array);
+//   PKV_BOX_BLOCK  3-D (64 columns, rows, D/64 panels at a 128-byte stride), a 64 x 16 x D/64 box:
+//                  the whole chunk in one copy, landing as [panel][16 rows][128 B] (the V tiles
+//                  of prefill, read by the tensor cores one 16-key block at a time).
+// Encoding goes through the driver entry point cuTensorMapEncodeTiled, found once through the
+// runtime; maps are cached by (address, shape, type, box, device) so steady-state calls do not
+// re-encode.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -20,6 +26,7 @@ struct MapEntry {
     long long rows;
     int head_dim;
     int dtype;
+    int box;
     int device;
     unsigned long long stamp;  // 0 = empty slot; else last use (least recently used is replaced)
     CUtensorMap map;
@@ -45,8 +52,10 @@ cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 
 }  // namespace
 
-cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, CUtensorMap* out) {
+cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, int box,
+                          CUtensorMap* out) {
     if (dtype != PKV_F16 && dtype != PKV_BF16) return cudaErrorInvalidValue;
+    if (box != PKV_BOX_PANEL && box != PKV_BOX_BLOCK) return cudaErrorInvalidValue;
     if (rows <= 0 || rows >= (1LL << 31) || (head_dim % 64) != 0) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -55,7 +64,7 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
     MapEntry* victim = &g_maps[0];
     for (MapEntry& e : g_maps) {
         if (e.stamp && e.base == layer_base && e.rows == rows && e.head_dim == head_dim && e.dtype == dtype &&
-            e.device == dev) {
+            e.box == box && e.device == dev) {
             e.stamp = ++g_clock;
             *out = e.map;
             return cudaSuccess;
@@ -65,20 +74,25 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     err = encoder(&encode);
     if (err != cudaSuccess) return err;
-    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
-    const cuuint32_t elem_strides[2] = {1, 1};
+    const bool blk = box == PKV_BOX_BLOCK;
+    const cuuint32_t rank = blk ? 3 : 2;
+    // dims / box innermost first; strides (bytes) of dims 1.. (the panel dim of the 3-D form steps
+    // 64 elements = 128 bytes inside a row)
+    const cuuint64_t dims[3] = {blk ? 64u : (cuuint64_t)head_dim, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128};
+    const cuuint32_t boxdim[3] = {64, (cuuint32_t)kBlock, (cuuint32_t)(head_dim / 64)};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
     CUtensorMap map;
-    CUresult r = encode(&map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                        const_cast<void*>(layer_base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = encode(&map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        rank, const_cast<void*>(layer_base), dims, strides, boxdim, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     victim->base = layer_base;
     victim->rows = rows;
     victim->head_dim = head_dim;
     victim->dtype = dtype;
+    victim->box = box;
     victim->device = dev;
     victim->stamp = ++g_clock;
     victim->map = map;
