@@ -224,3 +224,37 @@ def test_random_batches_stress(trial):
     if sum(new) == 0:
         new[0] = lens[0]
     check(dtype, lens, new, group * n_kv, n_kv, d, seed=2000 + trial)
+
+
+@pytest.mark.parametrize("d,group", [(256, 4), (128, 1)])
+def test_cuda_graph_replay_of_prefill(d, group):
+    """A captured prefill launch (clusters of four CTAs at head_dim 256) replays bit-identically
+    to the eager call, several times."""
+    import torch
+    dtype, n_kv = "bf16", 2
+    n_q = n_kv * group
+    q, kp, vp, tables, lens, qs = prefill_case(dtype, [700, 1300], [300, 500], n_q, n_kv, d, seed=77)
+    desc = pkv.make_desc(dtype, 1, kp.shape[1], n_q, n_kv, d)
+    args = [to_torch(q, dtype), to_torch(kp, dtype), to_torch(vp, dtype),
+            torch.from_numpy(np.ascontiguousarray(tables, np.int32)).cuda(),
+            torch.from_numpy(np.ascontiguousarray(lens, np.int32)).cuda(),
+            torch.from_numpy(np.ascontiguousarray(qs, np.int32)).cuda()]
+    mql = int(np.max(np.diff(qs)))
+    scale = 1.0 / np.sqrt(d)
+    eager = torch.empty_like(args[0])
+    pkv.pkv_paged_prefill_attention(desc, 0, args[0], args[1], args[2], args[3], args[4], args[5], mql, scale, eager)
+    out = torch.zeros_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pkv.pkv_paged_prefill_attention(desc, 0, args[0], args[1], args[2], args[3], args[4], args[5], mql, scale,
+                                        out)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pkv.pkv_get_device_status() == 0
+    want = oracle.paged_prefill(dtype, q, kp[0], vp[0], tables, lens, qs, scale, n_threads=THREADS)
+    assert np.max(np.abs(as_f64(out) - want)) <= TOL[dtype]
