@@ -1,7 +1,7 @@
 """Benchmark: paged decode attention on one GB300 (KV GB/s, decode tokens/s, % of HBM roofline).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gpt|ragged|longdoc|prefix|prefill30k]
-                    [--impl pkv|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--config gpt|ragged|longdoc|prefix|prefill30k|serve|appendcopy] [--impl pkv|reference]
 
 A step is one decode step of the whole hot path over one batch: the host block manager
 reserves a slot per sequence (copy-on-write pairs included), the metadata goes to the device,
@@ -13,6 +13,9 @@ the outputs copied back inside the timed region.
 
 --config prefill30k prints the chunked-prefill line instead: one 30,000-token prompt of the
 long-document model prefilled in chunks of 2,048 tokens, ``value`` = causal attention TFLOP/s.
+--config appendcopy times the two copy kernels of the path alone: per step one copy_blocks of 200
+copy-on-write pairs over all layers and one kv_append per layer for a batch of 64 tokens;
+``value`` = bytes read + written per step / step time.
 
 Every input is synthetic and seeded (see paged_kv_cache_258_gb300/workloads.py). Multi-GPU
 (torchrun) runs one independent replica per rank (weak scaling: sequences shard across ranks
@@ -634,26 +637,31 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
             "ms_per_step": round(ms / args.steps, 4)}
 
 
-def traffic_per_launch(config: str, algorithmic: float):
-    """DRAM bytes per decode launch from the committed ncu capture, if it matches this kernel."""
-    f = ROOT / "profiles" / f"paged_decode_{config}.traffic.json"
+DECODE_SOURCES = ("decode.cuh", "decode_mma.cuh", "common.cuh")
+COPY_SOURCES = ("append_copy.cu", "common.cuh")
+
+
+def traffic_per_launch(config: str, algorithmic: float, profile: str | None = None,
+                       sources: tuple = DECODE_SOURCES):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the kernel as built now."""
+    f = ROOT / "profiles" / (profile or f"paged_decode_{config}.traffic.json")
     if not f.exists():
         return None
     try:
         rec = json.loads(f.read_text())
     except ValueError:
         return None
-    if rec.get("kernel_source_sha256") != kernel_source_hash():
+    if rec.get("kernel_source_sha256") != kernel_source_hash(sources):
         return None  # the kernel changed since the counters were taken
     ratio = rec.get("dram_bytes_per_algorithmic_byte")
     return None if ratio is None else int(ratio * algorithmic)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources: tuple = DECODE_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "paged_kv_cache_258_gb300" / "csrc"
-    for name in ("decode.cuh", "decode_mma.cuh", "common.cuh"):
+    for name in sources:
         h.update((csrc / name).read_bytes())
     return h.hexdigest()
 
@@ -918,6 +926,225 @@ def run_serve_gpu(args) -> dict | None:
     return line
 
 
+# ---------------------------------------------------------------------------------------------
+# the copy kernels alone: copy-on-write block copies ("01 - Conceito", paragraph 6: 200 pairs, as
+# when every member of the prefix-sharing workload first writes into its shared tail block) over the
+# GPT-style model's 32 layers, and the per-layer KV append of a 64-token decode batch ("La idea de
+# PagedAttention", step 3)
+
+APPEND_COPY_METRIC = "KV append + copy-on-write block copy: GB/s moved (read + write) at 1 GB300; % of HBM roofline"
+AC = dict(n_layers=32, n_q=32, n_kv=32, d=128, dtype="f16", num_blocks=2048, batch=64, pairs=200,
+          seed=W.BASE_SEED + 7)
+
+
+def append_copy_bytes(P) -> tuple[int, int]:
+    """Bytes read + written per step by copy_blocks and by the layer loop of kv_append."""
+    row = P["n_kv"] * P["d"] * 2  # one token's K (or V) row of one layer, fp16
+    copy = P["pairs"] * P["n_layers"] * row * W.BLOCK * 2 * 2  # K and V, read and write
+    append = P["batch"] * P["n_layers"] * row * 2 * 2
+    return copy, append
+
+
+def append_copy_inputs(P, n_steps: int):
+    """Seeded per-step slots (distinct within a step) and the fixed copy pairs (disjoint src / dst)."""
+    rng = np.random.default_rng(P["seed"])
+    half = P["num_blocks"] // 2
+    src = rng.permutation(half)[: P["pairs"]]
+    dst = half + rng.permutation(half)[: P["pairs"]]
+    pairs = np.stack([src, dst], axis=1).astype(np.int32)
+    slots = np.stack([rng.permutation(P["num_blocks"] * W.BLOCK)[: P["batch"]] for _ in range(n_steps)])
+    return pairs, slots.astype(np.int64)
+
+
+def run_append_copy_gpu(args) -> dict | None:
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pkv.lib()
+    P = dict(AC, n_layers=args.layers) if args.layers else AC
+    L = P["n_layers"]
+    desc = pkv.make_desc(P["dtype"], L, P["num_blocks"], P["n_q"], P["n_kv"], P["d"])
+    g = torch.Generator(device=device)
+    g.manual_seed(P["seed"] + rank)
+    kp = torch.empty(pkv.pool_shape(desc), dtype=torch.float16, device=device).normal_(generator=g)
+    vp = torch.empty_like(kp).normal_(generator=g)
+    k_new = torch.empty((L, P["batch"], P["n_kv"], P["d"]), dtype=torch.float16, device=device).normal_(generator=g)
+    v_new = torch.empty_like(k_new).normal_(generator=g)
+    n_steps = args.warmup + 3 * args.steps
+    pairs_h, slots_h = append_copy_inputs(P, n_steps)
+    pairs = torch.from_numpy(pairs_h).to(device)
+    slots = torch.from_numpy(slots_h).to(device)
+    stream = torch.cuda.current_stream()
+    copy_b, append_b = append_copy_bytes(P)
+
+    def one_step(i, ev=None, host=None):
+        kn, vn, sl, pr = k_new, v_new, slots[i], pairs
+        if host is not None:  # the step's inputs from pinned host memory
+            hk, hv, hsl, hpr, dk, dv, dsl, dpr = host
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dsl.copy_(hsl[i], non_blocking=True)
+            dpr.copy_(hpr, non_blocking=True)
+            kn, vn, sl, pr = dk, dv, dsl, dpr
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.pkv_copy_blocks(desc, kp, vp, pr)  # copies first, then the new rows (step order)
+        if ev is not None:
+            ev[1].record(stream)
+        for layer in range(L):
+            pkv.pkv_kv_append(desc, layer, kn[layer], vn[layer], sl, kp, vp)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        one_step(i)
+    if pkv.pkv_get_device_status():
+        raise RuntimeError("device status flags during warm-up")
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_uuid(local))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = pkv.pkv_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for j in range(args.steps):  # value: the steps alone
+        one_step(args.warmup + j)
+    t1.record(stream)
+    for j in range(args.steps):  # roofline: the same kind of steps with events around each kernel group
+        one_step(args.warmup + args.steps + j, evs[j])
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = (pkv.pkv_launch_count() - launches0) // 2
+    if pkv.pkv_get_device_status():
+        raise RuntimeError("device status flags set during the timed region")
+    ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
+    copy_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    append_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+
+    # e2e: new rows, slots and pairs from pinned host memory each step; one destination block of
+    # layer 0 read back (the copy's result) at the end of every step
+    host = (k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), torch.from_numpy(slots_h).pin_memory(),
+            torch.from_numpy(pairs_h).pin_memory(), torch.empty_like(k_new), torch.empty_like(v_new),
+            torch.empty(P["batch"], dtype=torch.int64, device=device), torch.empty_like(pairs))
+    back = torch.empty(kp[0, 0].shape, dtype=kp.dtype).pin_memory()
+    dst0 = int(pairs_h[0, 1])
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for j in range(args.steps):
+        one_step(args.warmup + 2 * args.steps + j, host=host)
+        back.copy_(kp[0, dst0], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", device)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    peak_src = "measured hbm_gbs (copy bandwidth, read + write bytes)" if "hbm_gbs" in peaks \
+        else f"fallback {FALLBACK_HBM_GBS:.0f} GB/s"
+    step_bytes = copy_b + append_b
+    value = step_bytes * args.steps * ws / (ms * 1e-3) / 1e9
+    achieved = copy_b / (copy_ms * 1e-3) / 1e9
+    h2d = (k_new.numel() + v_new.numel()) * 2 + P["batch"] * 8 + pairs.numel() * 4
+    line = {
+        "metric": APPEND_COPY_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) pools and rows; seeded slots and pairs)",
+        "config": {"workload": f"appendcopy: copy_blocks of {P['pairs']} copy-on-write pairs over {L} layers "
+                               f"(K and V) + kv_append of a {P['batch']}-token batch into each of {L} layers; "
+                               f"{P['n_kv']} kv heads x head_dim {P['d']} fp16, block 16, {P['num_blocks']} blocks",
+                   "l2": "no flush: each step copies 1.68 GB of distinct blocks (larger than L2)",
+                   "parallelism": f"replicas x{ws} (one pool per rank, no collective)"},
+        "roofline": {"kernel": "copy_blocks_kernel (16-byte vector copies, grid pair x layer x K/V)",
+                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_per_launch("appendcopy", copy_b, "copy_blocks_appendcopy.traffic.json",
+                                                   COPY_SOURCES),
+                     "launch_ms_mean": round(copy_ms, 5), "algorithmic_bytes_per_launch": int(copy_b)},
+        "append": {"kernel": "kv_append_kernel", "launches_per_step": L,
+                   "us_per_launch": round(append_ms / L * 1e3, 3),
+                   "gbs": round(append_b / (append_ms * 1e-3) / 1e9, 2),
+                   "bytes_per_launch": int(append_b // L)},
+        "e2e": {"value": round(step_bytes * args.steps * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(back.numel() * 2),
+                "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = append_copy_cpu_sample(budget_s=args.cpu_budget)
+    return line
+
+
+_AC_HOST = {}
+
+
+def append_copy_cpu_sample(budget_s: float = 10.0, layers: int = 2) -> dict:
+    """The oracle's copy_blocks and kv_append (plain byte copies) on host pools of `layers` layers."""
+    import oracle
+    oracle.build()
+    P = dict(AC, n_layers=layers)
+    if layers not in _AC_HOST:  # host pools built once per process (their bits do not matter to a copy)
+        rng = np.random.default_rng(P["seed"])
+        shape = (layers, P["num_blocks"], P["n_kv"], W.BLOCK, P["d"])
+        kp = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16).view(np.float16)
+        vp = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16).view(np.float16)
+        kn = rng.standard_normal((P["batch"], P["n_kv"], P["d"]), dtype=np.float32).astype(np.float16)
+        vn = rng.standard_normal((P["batch"], P["n_kv"], P["d"]), dtype=np.float32).astype(np.float16)
+        pairs, slots = append_copy_inputs(P, 64)
+        _AC_HOST[layers] = (kp, vp, kn, vn, pairs, slots)
+    kp, vp, kn, vn, pairs, slots = _AC_HOST[layers]
+    copy_b, append_b = append_copy_bytes(P)
+    done, el, steps = 0, 0.0, 0
+    while el < budget_s and steps < 10_000:
+        t0 = time.perf_counter()
+        oracle.copy_blocks(kp, vp, pairs)
+        for layer in range(layers):
+            oracle.kv_append(kn, vn, slots[steps % len(slots)], kp[layer], vp[layer])
+        el += time.perf_counter() - t0
+        done += copy_b + append_b
+        steps += 1
+    return {"value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} steps of the same work on {layers} of {AC['n_layers']} layers "
+                      f"(fp16 byte copies in the C oracle, one thread); {el:.1f} s"}
+
+
+def run_append_copy_reference(args) -> dict | None:
+    """Reference arm of the appendcopy line: the oracle's byte copies, as they stand, on the host."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    per_step = max(0.5, 60.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        append_copy_cpu_sample(budget_s=per_step / 4)
+    t0 = time.perf_counter()
+    samples = [append_copy_cpu_sample(budget_s=per_step) for _ in range(args.steps)]
+    el = time.perf_counter() - t0
+    value = statistics.median(s_["value"] for s_ in samples)
+    cb = dict(samples[0])
+    cb["value"] = value
+    return {
+        "impl": "reference", "metric": APPEND_COPY_METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "appendcopy (bounded sample: 2 of 32 layers)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_prefill_reference(args) -> dict | None:
     """Reference arm of the prefill line: the fp64 oracle, as it stands, on a bounded sample."""
     ws, rank, _ = dist_env()
@@ -951,7 +1178,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="gpt",
-                    choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k", "serve"])
+                    choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k", "serve", "appendcopy"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
@@ -966,6 +1193,8 @@ def main(argv=None):
     if args.impl == "reference":
         if args.config == "prefill30k":
             line = run_prefill_reference(args)
+        elif args.config == "appendcopy":
+            line = run_append_copy_reference(args)
         elif args.config == "serve":
             line = {"impl": "reference", "unavailable": "the serving loop has no CPU restatement: its kernels' "
                                                        "reference arms are --config gpt and --config prefill30k"}
@@ -973,6 +1202,8 @@ def main(argv=None):
             line = run_reference(args)
     elif args.config == "prefill30k":
         line = run_prefill_gpu(args)
+    elif args.config == "appendcopy":
+        line = run_append_copy_gpu(args)
     elif args.config == "serve":
         line = run_serve_gpu(args)
     else:
