@@ -981,22 +981,38 @@ def run_append_copy_gpu(args) -> dict | None:
     stream = torch.cuda.current_stream()
     copy_b, append_b = append_copy_bytes(P)
 
+    # The 32 appends of a step (~1-2 us of GPU work each) are replayed from a CUDA graph, as a
+    # serving loop would issue them: launched one by one from Python they wait on the host. The
+    # graph reads the step's slots from a fixed buffer that each step refills on the device.
+    slot_buf = torch.empty(P["batch"], dtype=torch.int64, device=device)
+    slot_buf.copy_(slots[0])
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):  # one eager pass on the capture stream before capturing
+        for layer in range(L):
+            pkv.pkv_kv_append(desc, layer, k_new[layer], v_new[layer], slot_buf, kp, vp)
+    stream.wait_stream(cap)
+    append_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(append_graph, stream=cap):
+        for layer in range(L):
+            pkv.pkv_kv_append(desc, layer, k_new[layer], v_new[layer], slot_buf, kp, vp)
+    torch.cuda.synchronize()
+
     def one_step(i, ev=None, host=None):
-        kn, vn, sl, pr = k_new, v_new, slots[i], pairs
-        if host is not None:  # the step's inputs from pinned host memory
-            hk, hv, hsl, hpr, dk, dv, dsl, dpr = host
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            dsl.copy_(hsl[i], non_blocking=True)
-            dpr.copy_(hpr, non_blocking=True)
-            kn, vn, sl, pr = dk, dv, dsl, dpr
+        if host is not None:  # the step's inputs from pinned host memory into the buffers the graph reads
+            hk, hv, hsl, hpr = host
+            k_new.copy_(hk, non_blocking=True)
+            v_new.copy_(hv, non_blocking=True)
+            slot_buf.copy_(hsl[i], non_blocking=True)
+            pairs.copy_(hpr, non_blocking=True)
+        else:
+            slot_buf.copy_(slots[i])
         if ev is not None:
             ev[0].record(stream)
-        pkv.pkv_copy_blocks(desc, kp, vp, pr)  # copies first, then the new rows (step order)
+        pkv.pkv_copy_blocks(desc, kp, vp, pairs)  # copies first, then the new rows (step order)
         if ev is not None:
             ev[1].record(stream)
-        for layer in range(L):
-            pkv.pkv_kv_append(desc, layer, kn[layer], vn[layer], sl, kp, vp)
+        append_graph.replay()
         if ev is not None:
             ev[2].record(stream)
 
@@ -1022,7 +1038,8 @@ def run_append_copy_gpu(args) -> dict | None:
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    launches = (pkv.pkv_launch_count() - launches0) // 2
+    # copy_blocks launches counted by the library, plus the appends each graph replay runs
+    launches = (pkv.pkv_launch_count() - launches0) // 2 + args.steps * L
     if pkv.pkv_get_device_status():
         raise RuntimeError("device status flags set during the timed region")
     ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
@@ -1032,8 +1049,7 @@ def run_append_copy_gpu(args) -> dict | None:
     # e2e: new rows, slots and pairs from pinned host memory each step; one destination block of
     # layer 0 read back (the copy's result) at the end of every step
     host = (k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), torch.from_numpy(slots_h).pin_memory(),
-            torch.from_numpy(pairs_h).pin_memory(), torch.empty_like(k_new), torch.empty_like(v_new),
-            torch.empty(P["batch"], dtype=torch.int64, device=device), torch.empty_like(pairs))
+            torch.from_numpy(pairs_h).pin_memory())
     back = torch.empty(kp[0, 0].shape, dtype=kp.dtype).pin_memory()
     dst0 = int(pairs_h[0, 1])
     torch.cuda.synchronize()
@@ -1072,7 +1088,7 @@ def run_append_copy_gpu(args) -> dict | None:
                      "traffic": traffic_per_launch("appendcopy", copy_b, "copy_blocks_appendcopy.traffic.json",
                                                    COPY_SOURCES),
                      "launch_ms_mean": round(copy_ms, 5), "algorithmic_bytes_per_launch": int(copy_b)},
-        "append": {"kernel": "kv_append_kernel", "launches_per_step": L,
+        "append": {"kernel": "kv_append_kernel", "launches_per_step": L, "issued": "CUDA graph replay",
                    "us_per_launch": round(append_ms / L * 1e3, 3),
                    "gbs": round(append_b / (append_ms * 1e-3) / 1e9, 2),
                    "bytes_per_launch": int(append_b // L)},

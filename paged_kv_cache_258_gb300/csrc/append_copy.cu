@@ -54,7 +54,22 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a) {
     const uint4* s = reinterpret_cast<const uint4*>(pool + (size_t)src * a.block_bytes);
     uint4* d = reinterpret_cast<uint4*>(pool + (size_t)dst * a.block_bytes);
     const size_t n = a.block_bytes / 16;
-    for (size_t i = threadIdx.x; i < n; i += blockDim.x) d[i] = s[i];
+    // eight 16-byte loads in flight per thread before their stores: source and destination lie in
+    // the same pool, so a plain load-store loop would keep only one load outstanding
+    constexpr int U = 8;
+    for (size_t i0 = threadIdx.x; i0 < n; i0 += (size_t)U * blockDim.x) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t i = i0 + (size_t)u * blockDim.x;
+            if (i < n) r[u] = s[i];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t i = i0 + (size_t)u * blockDim.x;
+            if (i < n) d[i] = r[u];
+        }
+    }
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
