@@ -20,11 +20,62 @@ All device work is in libpkv's kernels; this module only moves arguments.
 from __future__ import annotations
 
 import ctypes
+import os
 import time
 
 import numpy as np
 
 from . import pkv
+
+# PKV_CHECK=1: every planned step's metadata is validated on the host before it is uploaded (the
+# kernels skip and flag bad values anyway; this names the offending entry before any launch).
+CHECK_METADATA = os.environ.get("PKV_CHECK") == "1"
+
+
+def validate_step_metadata(num_blocks: int, block_size: int, tables, lens, slots=None, pairs=None) -> None:
+    """Host-side check of one step's device arguments; raises ValueError naming the first bad entry.
+
+    tables [n, max_blocks] int32 and lens [n]: every block a sequence uses (the first ceil(len / 16)
+    entries of its row) lies in [0, num_blocks) and len <= max_blocks * block_size; slots [n]: each in
+    [0, num_blocks * block_size) or negative (skipped), no two equal, and each in the last block of its
+    sequence's table at offset (len - 1) % block_size; pairs [p, 2]: source and destination ids in
+    range, destinations distinct and disjoint from the sources (copy_blocks' contract).
+    """
+    tables = np.asarray(tables)
+    lens = np.asarray(lens)
+    n, mb = tables.shape
+    if lens.shape != (n,):
+        raise ValueError(f"lens has shape {lens.shape}, expected ({n},)")
+    for s in range(n):
+        ln = int(lens[s])
+        if ln < 0 or ln > mb * block_size:
+            raise ValueError(f"sequence {s}: length {ln} outside [0, {mb * block_size}]")
+        used = tables[s, : -(-ln // block_size)]
+        bad = np.nonzero((used < 0) | (used >= num_blocks))[0]
+        if len(bad):
+            i = int(bad[0])
+            raise ValueError(f"sequence {s}: table entry {i} = {int(used[i])} outside [0, {num_blocks})")
+    if slots is not None:
+        slots = np.asarray(slots)
+        live = slots[slots >= 0]
+        if np.any(live >= num_blocks * block_size):
+            raise ValueError(f"slot {int(live[live >= num_blocks * block_size][0])} beyond the pool")
+        if len(np.unique(live)) != len(live):
+            raise ValueError("two tokens share one slot")
+        for s in range(min(n, len(slots))):
+            if slots[s] < 0 or lens[s] <= 0:
+                continue
+            ln = int(lens[s])
+            want = int(tables[s, (ln - 1) // block_size]) * block_size + (ln - 1) % block_size
+            if int(slots[s]) != want:
+                raise ValueError(f"sequence {s}: slot {int(slots[s])} is not position {ln - 1} of its table ({want})")
+    if pairs is not None and len(pairs):
+        pairs = np.asarray(pairs).reshape(-1, 2)
+        if np.any((pairs < 0) | (pairs >= num_blocks)):
+            raise ValueError("copy pair with a block id outside the pool")
+        src, dst = set(pairs[:, 0].tolist()), pairs[:, 1].tolist()
+        if len(set(dst)) != len(dst) or src & set(dst):
+            raise ValueError("copy pairs: destinations repeat or overlap the sources")
 
 
 class PagedKVCache:
@@ -154,6 +205,9 @@ class DecodeBatch:
             raise pkv.PkvError(rc, "pack_tables (is max_blocks wide enough?)")
         st["npairs"] = npairs
         self.manager_s += time.perf_counter() - t0
+        if CHECK_METADATA:
+            validate_step_metadata(self.cache.desc.num_blocks, self.cache.desc.block_size, st["tables"].numpy(),
+                                   st["np_lens"], st["slots"].numpy(), st["pairs"].numpy()[:npairs])
         self.steps_planned += 1
         self.last_lens = st["np_lens"].copy()
         self.last_n_pairs = npairs

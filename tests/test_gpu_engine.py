@@ -23,7 +23,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("dtype,n_q,n_kv,d", [("f16", 4, 4, 64), ("bf16", 8, 2, 128), ("f32", 4, 1, 64)])
-def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d, fused):
+def test_prefix_churn_steps_match_oracle(dtype, n_q, n_kv, d, fused, monkeypatch):
+    # every planned step also passes the host-side metadata check (no false alarms on real steps)
+    from paged_kv_cache_258_gb300 import engine
+    monkeypatch.setattr(engine, "CHECK_METADATA", True)
     rng = np.random.default_rng(77)
     L, n_groups, n_members, n_steps = 2, 3, 12, 24
     prompts = [int(100 + rng.integers(1, 16)) for _ in range(n_groups)]   # partial shared tails
