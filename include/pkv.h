@@ -390,6 +390,27 @@ int32_t pkv_mgr_free_list(const pkv_mgr* mgr, int32_t* out, int32_t cap);
  */
 int pkv_mgr_inject_alloc_failure(pkv_mgr* mgr, int32_t after_n_allocs);
 
+/*
+ * Checkpoint / resume of the host manager (the pages have no counterpart; the device pools are
+ * caller-owned tensors and are saved by the caller). The image is a little-endian byte string:
+ * "PKVM", version 1, num_blocks, block_size, the free list front first, the four event counters
+ * of pkv_stats, then every sequence in ascending id order (id, context length, block count,
+ * table), then an FNV-1a 64 checksum of everything before it. Reference counts are not stored:
+ * a block's count is the number of tables that hold it. The fault-injection setting is not saved.
+ *
+ * pkv_mgr_save_bytes: the size of the image of the current state (0 if mgr is NULL).
+ * pkv_mgr_save: write it into buf (host, cap bytes); *written receives its size.
+ *   PKV_ERR_INVALID_ARG if an argument is NULL or cap is too small (nothing written).
+ * pkv_mgr_load: a new manager whose state equals the saved one (same tables, lengths, free-list
+ *   order, reference counts and counters; every later operation gives the same results as on the
+ *   saved manager), or NULL if the image is malformed: wrong magic, version, size or checksum, an
+ *   id out of range, a block both free and referenced or neither, a table whose length does not
+ *   match its context, a repeated sequence id.
+ */
+size_t pkv_mgr_save_bytes(const pkv_mgr* mgr);
+int pkv_mgr_save(const pkv_mgr* mgr, void* buf, size_t cap, size_t* written);
+pkv_mgr* pkv_mgr_load(const void* buf, size_t len);
+
 #ifdef __cplusplus
 }
 #endif

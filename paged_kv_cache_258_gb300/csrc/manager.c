@@ -525,3 +525,157 @@ int pkv_mgr_inject_alloc_failure(pkv_mgr* m, int32_t after_n_allocs) {
     m->inject_after = after_n_allocs < 0 ? -1 : after_n_allocs;
     return PKV_OK;
 }
+
+/* ---- checkpoint / resume ------------------------------------------------------------------ */
+
+#define PKV_IMG_MAGIC 0x4d564b50u /* "PKVM" little-endian */
+#define PKV_IMG_VERSION 1u
+
+static uint64_t fnv1a64(const uint8_t* p, size_t n) {
+    uint64_t h = 0xcbf29ce484222325ull;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 0x100000001b3ull;
+    }
+    return h;
+}
+
+static void put_u32(uint8_t** w, uint32_t v) {
+    for (int i = 0; i < 4; ++i) *(*w)++ = (uint8_t)(v >> (8 * i));
+}
+static void put_u64(uint8_t** w, uint64_t v) {
+    for (int i = 0; i < 8; ++i) *(*w)++ = (uint8_t)(v >> (8 * i));
+}
+static uint32_t get_u32(const uint8_t** r) {
+    uint32_t v = 0;
+    for (int i = 0; i < 4; ++i) v |= (uint32_t)(*(*r)++) << (8 * i);
+    return v;
+}
+static uint64_t get_u64(const uint8_t** r) {
+    uint64_t v = 0;
+    for (int i = 0; i < 8; ++i) v |= (uint64_t)(*(*r)++) << (8 * i);
+    return v;
+}
+
+size_t pkv_mgr_save_bytes(const pkv_mgr* m) {
+    if (!m) return 0;
+    size_t n = 4 + 4 + 4 + 4 + 4 + (size_t)m->n_free * 4 + 4 * 8 + 8;
+    for (int64_t i = 0; i < m->map_cap; ++i)
+        if (m->map[i].used) n += 8 + 4 + 4 + (size_t)m->map[i].n_blocks * 4;
+    return n + 8;
+}
+
+static int cmp_id(const void* a, const void* b) {
+    const int64_t x = (*(const seq_rec* const*)a)->id, y = (*(const seq_rec* const*)b)->id;
+    return x < y ? -1 : (x > y);
+}
+
+int pkv_mgr_save(const pkv_mgr* m, void* buf, size_t cap, size_t* written) {
+    if (!m || !buf || !written) return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv_mgr_save_bytes(m);
+    if (cap < need) return PKV_ERR_INVALID_ARG;
+    const seq_rec** order = NULL;
+    if (m->n_seqs > 0) {
+        order = (const seq_rec**)malloc(sizeof(seq_rec*) * (size_t)m->n_seqs);
+        if (!order) return PKV_ERR_INVALID_ARG;
+        int64_t k = 0;
+        for (int64_t i = 0; i < m->map_cap; ++i)
+            if (m->map[i].used) order[k++] = &m->map[i];
+        qsort(order, (size_t)m->n_seqs, sizeof(seq_rec*), cmp_id);
+    }
+    uint8_t* w = (uint8_t*)buf;
+    put_u32(&w, PKV_IMG_MAGIC);
+    put_u32(&w, PKV_IMG_VERSION);
+    put_u32(&w, (uint32_t)m->num_blocks);
+    put_u32(&w, (uint32_t)m->block_size);
+    put_u32(&w, (uint32_t)m->n_free);
+    for (int32_t i = 0; i < m->n_free; ++i) put_u32(&w, (uint32_t)m->ring[(m->head + i) % m->num_blocks]);
+    put_u64(&w, (uint64_t)m->alloc_failures);
+    put_u64(&w, (uint64_t)m->prefix_hits);
+    put_u64(&w, (uint64_t)m->cow_copies);
+    put_u64(&w, (uint64_t)m->append_oom);
+    put_u64(&w, (uint64_t)m->n_seqs);
+    for (int64_t k = 0; k < m->n_seqs; ++k) {
+        const seq_rec* r = order[k];
+        put_u64(&w, (uint64_t)r->id);
+        put_u32(&w, (uint32_t)r->ctx);
+        put_u32(&w, (uint32_t)r->n_blocks);
+        for (int32_t b = 0; b < r->n_blocks; ++b) put_u32(&w, (uint32_t)r->table[b]);
+    }
+    free(order);
+    put_u64(&w, fnv1a64((const uint8_t*)buf, (size_t)(w - (uint8_t*)buf)));
+    *written = (size_t)(w - (uint8_t*)buf);
+    return PKV_OK;
+}
+
+pkv_mgr* pkv_mgr_load(const void* buf, size_t len) {
+    if (!buf || len < 4 + 4 + 4 + 4 + 4 + 5 * 8 + 8) return NULL;
+    const uint8_t* base = (const uint8_t*)buf;
+    const uint8_t* end = base + len - 8;
+    const uint8_t* sum_at = end;
+    if (get_u64(&sum_at) != fnv1a64(base, len - 8)) return NULL;
+    const uint8_t* r = base;
+    if (get_u32(&r) != PKV_IMG_MAGIC || get_u32(&r) != PKV_IMG_VERSION) return NULL;
+    const int32_t num_blocks = (int32_t)get_u32(&r);
+    const int32_t block_size = (int32_t)get_u32(&r);
+    const int32_t n_free = (int32_t)get_u32(&r);
+    if (num_blocks <= 0 || block_size <= 0 || n_free < 0 || n_free > num_blocks) return NULL;
+    if ((size_t)(end - r) < (size_t)n_free * 4 + 5 * 8) return NULL;
+    pkv_mgr* m = pkv_mgr_create(num_blocks, block_size, NULL);
+    if (!m) return NULL;
+    /* free list, front first; ref[] temporarily marks "free" with -1 */
+    for (int32_t i = 0; i < n_free; ++i) {
+        const int32_t b = (int32_t)get_u32(&r);
+        if (b < 0 || b >= num_blocks || m->ref[b] != 0) goto bad;
+        m->ref[b] = -1;
+        m->ring[i] = b;
+    }
+    m->head = 0;
+    m->n_free = n_free;
+    m->alloc_failures = (int64_t)get_u64(&r);
+    m->prefix_hits = (int64_t)get_u64(&r);
+    m->cow_copies = (int64_t)get_u64(&r);
+    m->append_oom = (int64_t)get_u64(&r);
+    const int64_t n_seqs = (int64_t)get_u64(&r);
+    if (n_seqs < 0) goto bad;
+    for (int64_t k = 0; k < n_seqs; ++k) {
+        if ((size_t)(end - r) < 16) goto bad;
+        const int64_t id = (int64_t)get_u64(&r);
+        const int32_t ctx = (int32_t)get_u32(&r);
+        const int32_t nb = (int32_t)get_u32(&r);
+        if (ctx < 0 || nb < 0 || nb != (int32_t)(((int64_t)ctx + block_size - 1) / block_size)) goto bad;
+        if ((size_t)(end - r) < (size_t)nb * 4) goto bad;
+        if (map_find(m, id) >= 0 || !map_reserve_one(m)) goto bad;
+        int32_t* table = NULL;
+        if (nb > 0) {
+            table = (int32_t*)malloc(sizeof(int32_t) * (size_t)nb);
+            if (!table) goto bad;
+        }
+        for (int32_t b = 0; b < nb; ++b) {
+            const int32_t id_b = (int32_t)get_u32(&r);
+            if (id_b < 0 || id_b >= num_blocks || m->ref[id_b] < 0) {
+                free(table);
+                goto bad;
+            }
+            table[b] = id_b;
+            m->ref[id_b]++;
+        }
+        seq_rec* rec = map_insert(m, id);
+        rec->table = table;
+        rec->n_blocks = nb;
+        rec->cap = nb;
+        rec->ctx = ctx;
+    }
+    if (r != end) goto bad;
+    /* every block is either free or held by some table */
+    for (int32_t b = 0; b < num_blocks; ++b) {
+        if (m->ref[b] == 0) goto bad;
+        if (m->ref[b] < 0) m->ref[b] = 0;
+    }
+    return m;
+bad:
+    for (int32_t b = 0; b < num_blocks; ++b)
+        if (m->ref[b] < 0) m->ref[b] = 0;
+    pkv_mgr_destroy(m);
+    return NULL;
+}

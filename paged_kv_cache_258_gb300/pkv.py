@@ -96,6 +96,9 @@ def lib():
         "pkv_mgr_refcount": (c_i32, [vp, c_i32]),
         "pkv_mgr_free_list": (c_i32, [vp, i32p, c_i32]),
         "pkv_mgr_inject_alloc_failure": (ctypes.c_int, [vp, c_i32]),
+        "pkv_mgr_save_bytes": (c_sz, [vp]),
+        "pkv_mgr_save": (ctypes.c_int, [vp, vp, c_sz, ctypes.POINTER(c_sz)]),
+        "pkv_mgr_load": (vp, [vp, c_sz]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -351,6 +354,26 @@ class BlockManager:
         if not h:
             raise PkvError(PKV_ERR_BAD_STATE, "pkv_mgr_clone")
         return BlockManager(self.num_blocks, self.block_size, _handle=h)
+
+    def save(self) -> bytes:
+        """The manager's state as a pkv_mgr_save image (checkpoint)."""
+        L = lib()
+        n = int(L.pkv_mgr_save_bytes(self._h))
+        buf = ctypes.create_string_buffer(n)
+        written = ctypes.c_size_t(0)
+        _check(L.pkv_mgr_save(self._h, buf, n, ctypes.byref(written)), "pkv_mgr_save")
+        return buf.raw[: written.value]
+
+    @classmethod
+    def load(cls, image: bytes) -> "BlockManager":
+        """A manager resumed from a save() image; raises PkvError if the image is malformed."""
+        data = bytes(image)
+        h = lib().pkv_mgr_load(data, len(data))
+        if not h:
+            raise PkvError(PKV_ERR_INVALID_ARG, "pkv_mgr_load (malformed image)")
+        num_blocks = int.from_bytes(data[8:12], "little")
+        block_size = int.from_bytes(data[12:16], "little")
+        return cls(num_blocks, block_size, _handle=h)
 
     def add_seq(self, seq_id: int, n_prompt: int, reserve_tokens: int = 0):
         slots = np.zeros(max(int(n_prompt), 1), dtype=np.int64)
