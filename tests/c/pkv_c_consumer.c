@@ -9,7 +9,9 @@
  *   3. one decode step: pkv_mgr_append_slot reserves each sequence's next slot, then
  *      pkv_paged_decode_append_attention appends the new rows and attends in one call (step 5);
  *   4. the result is compared with the fp64 oracle (oracle/oracle.c, test infrastructure) run on
- *      host copies of the same rows, written through the oracle's own append.
+ *      host copies of the same rows, written through the oracle's own append;
+ *   5. the manager is saved and reloaded (pkv_mgr_save / pkv_mgr_load) and must carry on exactly
+ *      like the original.
  * Exit status 0 and a line "c consumer ok" on success; the largest |gpu - oracle| must stay within
  * 2e-2 (fp16 inputs, fp32 accumulation), and the device status word must read 0.
  */
@@ -182,6 +184,29 @@ int main(void) {
             }
         }
     }
+    /* 5. checkpoint / resume: a manager reloaded from its saved image packs the same tables and
+     *    hands out the same next slots as the original */
+    const size_t img_bytes = pkv_mgr_save_bytes(mgr);
+    unsigned char* img = malloc(img_bytes);
+    size_t written = 0;
+    CHECK(img != NULL && pkv_mgr_save(mgr, img, img_bytes, &written) == PKV_OK && written == img_bytes);
+    pkv_mgr* again = pkv_mgr_load(img, written);
+    CHECK(again != NULL);
+    int32_t tables2[3 * 8], lens2[3];
+    CHECK(pkv_mgr_pack_tables(again, ids, 3, max_blocks, tables2, lens2) == PKV_OK);
+    CHECK(memcmp(tables, tables2, sizeof tables) == 0 && memcmp(lens, lens2, sizeof lens) == 0);
+    for (int s = 0; s < 3; ++s) {
+        int64_t a = -1, b = -2;
+        int32_t s1, d1, s2, d2;
+        CHECK(pkv_mgr_append_slot(mgr, ids[s], &a, &s1, &d1) == PKV_OK);
+        CHECK(pkv_mgr_append_slot(again, ids[s], &b, &s2, &d2) == PKV_OK);
+        CHECK(a == b && s1 == s2 && d1 == d2);
+    }
+    img[written / 2] ^= 1u; /* a corrupted image is refused */
+    CHECK(pkv_mgr_load(img, written) == NULL);
+    free(img);
+    pkv_mgr_destroy(again);
+
     printf("c consumer ok: max |gpu - oracle| = %.3g over %d outputs\n", err, 3 * n_q * d);
     CHECK(err <= 2e-2);
     pkv_mgr_destroy(mgr);
