@@ -102,3 +102,55 @@ def test_prefill30k_fullsize_sampled():
                                     n_threads=oracle.max_threads())
         err = np.max(np.abs(got[layer, pos] - want))
         assert err <= TOL[dtype], f"layer {layer}: {err:.3e}"
+
+
+def test_prefix_fullsize_sampled():
+    """The prefix-sharing workload at full size (200 members forked from 8 roots, 5 % churn per
+    step, copy-on-write of each member's shared tail on its first write), in bench.py's launch
+    configuration. The Python manager oracle replays the same churn and appends; its copy-on-write
+    pairs and byte appends go into host copies of the pool; sampled members are checked."""
+    device = torch.device("cuda", 0)
+    wl, _, cache, batch, (q, kn, vn, out), state = bench.setup_gpu_case("prefix", WARMUP, STEPS, device)
+    dtype, churn, roots = wl.dtype, state["churn"], state["roots"]
+    host_k = np.ascontiguousarray(to_host(cache.k_pool[0], dtype)[None])  # [1, blocks, kv, 16, d]
+    host_v = np.ascontiguousarray(to_host(cache.v_pool[0], dtype)[None])
+    mo = BlockManagerOracle(wl.num_blocks, free_order=W.free_order(wl.num_blocks, wl.seed))
+    for g in range(churn.n_groups):
+        assert mo.add_seq(roots[g], churn.group_prompt[g])[0] == "ok"
+    for m, g in enumerate(churn.member_group):
+        assert mo.fork(roots[g], m) == "ok"
+    live = list(range(len(churn.member_group)))
+    n_cow = 0
+    for step in range(3):
+        if step < len(churn.steps):  # the same churn, in the same order, as bench.apply_churn
+            for old, new, g in churn.steps[step]:
+                assert mo.free_seq(old) == "ok" and mo.fork(roots[g], new) == "ok"
+                live[live.index(old)] = new
+        bench.apply_churn(cache, batch, state)
+        st = batch.step(q, kn, vn, out, wl.scale)
+        slots, pairs = [], []
+        for sid in live:  # append_batch = successive appends in batch order
+            status, slot, src, dst = mo.append_slot(sid)
+            assert status == "ok"
+            slots.append(slot)
+            if src >= 0:
+                pairs.append((src, dst))
+        assert st["slots"].numpy().tolist() == slots
+        n_cow += len(pairs)
+        if pairs:  # copies first, then the new rows (the step's order)
+            oracle.copy_blocks(host_k, host_v, np.array(pairs, dtype=np.int32))
+        oracle.kv_append(to_host(kn[0], dtype), to_host(vn[0], dtype), np.array(slots), host_k[0], host_v[0])
+    assert n_cow > 0
+    assert pkv.pkv_get_device_status() == 0
+    tables = np.full((len(live), batch.max_blocks), -1, dtype=np.int32)
+    lens = np.zeros(len(live), dtype=np.int32)
+    for i, sid in enumerate(live):
+        t, lens[i] = mo.block_table(sid)
+        tables[i, : len(t)] = t
+    assert np.array_equal(tables, st["tables"].numpy()) and np.array_equal(lens, st["lens"].numpy())
+    sel = np.array([0, 37, 101, 150, 199])
+    want = oracle.paged_decode(dtype, to_host(q[0], dtype)[sel], host_k[0], host_v[0], tables[sel], lens[sel],
+                               wl.scale, n_threads=oracle.max_threads())
+    err = np.max(np.abs(as_f64(out)[0][sel] - want))
+    assert err <= TOL[dtype], f"prefix: max abs error {err:.3e}"
+    assert torch.isfinite(out.float()).all()
