@@ -349,7 +349,8 @@ def run_gpu(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": wl.dtype,  # the operands of the QK^T and PV products (fp32 storage runs on CUDA cores)
+        "accumulate": "f32",
         "data": "synthetic (seeded N(0,1) K/V/q; shapes and length mixes of the pages' workloads)",
         "config": {
             "workload": wdesc,
@@ -543,7 +544,7 @@ def run_prefill_gpu(args) -> dict | None:
     line = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
         "data": "synthetic (seeded N(0,1) q and K/V rows)",
         "config": {"workload": f"prefill30k: one {prompt}-token prompt in {len(chunks)} chunks of {chunk} tokens, "
                                f"{L} layers x {n_q} q / {n_kv} kv heads x head_dim {d} bf16, block 16",
@@ -899,7 +900,7 @@ def run_serve_gpu(args) -> dict | None:
     line = {
         "metric": SERVE_METRIC, "value": round(tokens_all / wall_max, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(wall_max / max(steps, 1) * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": P["dtype"], "accumulate": "f32",
         "data": "synthetic (Poisson arrivals; seeded q and K/V rows; no model weights)",
         "config": {"workload": f"serve: {P['n_requests']} requests at {P['rate']}/s, 85% chat (prompt U{{64..512}}, "
                                f"response min(Geom(1/500), 2048), priority 1) / 15% doc (prompt U{{2048..8192}}, "
