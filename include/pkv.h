@@ -178,6 +178,24 @@ int pkv_paged_decode_append_attention(const pkv_cache_desc* desc, int32_t layer,
                                       const int32_t* context_lens, int32_t n_seqs, float scale, void* out,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pkv_paged_decode_append_attention with launch flags. PKV_DECODE_OVERLAP_PREVIOUS launches the
+ * kernel as a programmatic dependent of the previous kernel on `stream` (fp16 / bf16 storage; the
+ * flag has no effect for fp32): it may start while that kernel is finishing and read q, k_new,
+ * v_new, the tables, the lengths and layer `layer` of the pools before the previous kernel
+ * completes, and it writes the workspace, out and the status word only after. Set it only when
+ * the previous kernel on the stream writes none of those inputs -- in a decode step, the call for
+ * the previous layer with the same tables, lengths and workspace (its own out, k_new / v_new rows
+ * and pool layer are distinct). Unknown flag bits: PKV_ERR_INVALID_ARG. Results are bit-identical
+ * to pkv_paged_decode_append_attention.
+ */
+#define PKV_DECODE_OVERLAP_PREVIOUS 1u
+int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* desc, int32_t layer, const void* q,
+                                         const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t n_seqs, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes, uint32_t flags, void* stream);
+
 /* Size of the fixed scratch array used by pkv_paged_decode_attention_static (16 MiB). */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -171,7 +171,8 @@ int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const v
 }
 
 // Shared body of the two decode entry points; k_new / v_new are null unless the append is fused.
-static int decode_call(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new, const void* v_new,
+static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new,
+                       const void* v_new,
                        const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
                        const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
@@ -211,6 +212,7 @@ static int decode_call(const pkv_cache_desc* d, int32_t layer, const void* q, co
     a.n_parts = n_parts;
     a.bpp = bpp;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.overlap_previous = (flags & PKV_DECODE_OVERLAP_PREVIOUS) != 0 && d->dtype != PKV_F32;
     if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
     int launches = 0;
     cudaError_t err = pkv::launch_decode(d->dtype, d->head_dim, d->n_q_heads / d->n_kv_heads, a,
@@ -223,8 +225,8 @@ int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const voi
                                const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
                                size_t workspace_bytes, void* stream) {
-    return decode_call(d, layer, q, nullptr, nullptr, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
-                       n_seqs, scale, out, workspace, workspace_bytes, stream);
+    return decode_call(0u, d, layer, q, nullptr, nullptr, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                       context_lens, n_seqs, scale, out, workspace, workspace_bytes, stream);
 }
 
 int pkv_paged_decode_append_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new,
@@ -232,8 +234,19 @@ int pkv_paged_decode_append_attention(const pkv_cache_desc* d, int32_t layer, co
                                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
                                       float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
     if (n_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
-    return decode_call(d, layer, q, k_new, v_new, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+    return decode_call(0u, d, layer, q, k_new, v_new, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
                        n_seqs, scale, out, workspace, workspace_bytes, stream);
+}
+
+int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new,
+                                         const void* v_new, void* k_pool, void* v_pool, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t n_seqs,
+                                         float scale, void* out, void* workspace, size_t workspace_bytes,
+                                         uint32_t flags, void* stream) {
+    if (flags & ~(uint32_t)PKV_DECODE_OVERLAP_PREVIOUS) return PKV_ERR_INVALID_ARG;
+    if (n_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+    return decode_call(flags, d, layer, q, k_new, v_new, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                       context_lens, n_seqs, scale, out, workspace, workspace_bytes, stream);
 }
 
 int pkv_paged_prefill_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,

@@ -112,6 +112,10 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // Wait for the phase of `bar` with the given parity; false if it did not complete in time.
+// Wait until the grid this one was launched as a programmatic dependent of has completed and its
+// memory operations are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const int p = blockIdx.x;
     const int g = blockIdx.y;
     const int s = blockIdx.z;
+    // A launch that follows this one as a programmatic dependent (the next layer of the same
+    // decode step) may start once every CTA of this grid has passed here: its CTAs then fill the
+    // SMs this grid's tail leaves idle. Without such a launch this is a no-op.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // This warp's table entries of the partition (blocks p*bpp + warp + k*NW, k < kMaxBpp/NW <= 32),
     // loaded before the context length is known so the two global reads overlap; entries past the
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     const int b0 = p * a.bpp;
     if (b0 >= nb) {
         if (p == 0) {
+            grid_dependency_wait();
             T* o = reinterpret_cast<T*>(a.out) + ((size_t)s * a.n_q + (size_t)g * G) * D;
             for (int i = threadIdx.x; i < G * D; i += NW * 32) o[i] = from_float<T>(0.f);
         }
@@ -361,6 +366,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     }
 
     // ---- merge the warps ----
+    // Launched as a programmatic dependent, this grid may have streamed its keys while the previous
+    // kernel was finishing; the split-K workspace and the outputs are touched only once that kernel
+    // has completed and its writes are visible. Otherwise the wait returns at once.
+    grid_dependency_wait();
     __syncthreads();
     float* s_acc = reinterpret_cast<float*>(smem);  // [NW][8][D]
 #pragma unroll
@@ -442,8 +451,18 @@ cudaError_t launch_decode_mma_tpl(const DecodeArgs& a, const CUtensorMap& tk, co
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    dim3 grid(a.n_parts, a.n_kv, a.n_seqs);
-    kern<<<grid, NW * 32, smem, stream>>>(a, tk, tv);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_parts, a.n_kv, a.n_seqs);
+    cfg.blockDim = dim3(NW * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.overlap_previous ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
+    if (err != cudaSuccess) return err;
     if (n_launches) *n_launches = 1;
     return cudaGetLastError();
 }

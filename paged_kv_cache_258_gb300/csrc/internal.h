@@ -33,6 +33,7 @@ struct DecodeArgs {
     int n_parts;            // partitions per sequence row of the grid
     int bpp;                // blocks per partition
     float scale_log2;       // scale * log2(e): logits are kept in base 2
+    bool overlap_previous = false;  // launch as a programmatic dependent of the previous kernel
 };
 
 // Arguments of one paged prefill attention launch (one layer). q / out hold the chunk tokens of

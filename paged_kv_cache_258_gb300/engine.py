@@ -129,6 +129,8 @@ class DecodeBatch:
         self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
         # fused: one kernel per layer appends the new rows and attends; else kv_append + decode
         self.fused = bool(fused)
+        # overlap: each layer's fused launch may start while the previous layer's finishes
+        self.overlap = True
         dev = cache.device
         n, mb = self.n, self.max_blocks
         # One int32 metadata image per step, [slots (int64) | tables | lens | CoW pairs], so the
@@ -241,9 +243,14 @@ class DecodeBatch:
             if self.fused:
                 if on_decode is not None:
                     on_decode(layer, "start")
+                # layer l > 0 follows the previous layer's launch directly (no callback in between):
+                # it may start while that one finishes (they share only the tables, lengths and the
+                # workspace, which the kernel touches after the previous launch has completed)
                 pkv.pkv_paged_decode_append_attention(d, layer, q[layer], k_new[layer], v_new[layer], c.k_pool,
                                                       c.v_pool, self.d_tables, self.d_lens, scale, out[layer],
-                                                      self.workspace, stream=self.stream)
+                                                      self.workspace, stream=self.stream,
+                                                      overlap_previous=self.overlap and layer > 0
+                                                      and on_decode is None)
             else:
                 pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], self.d_slots, c.k_pool, c.v_pool,
                                   stream=self.stream)

@@ -19,6 +19,7 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_NO_BLOCKS, PKV_ERR_BAD
 STATUS_NAMES = {0: "ok", 1: "invalid", 2: "unsupported", 3: "no_blocks", 4: "bad_state", 5: "cuda"}
 PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT_LEN, PKV_DEV_BAD_SLOT, PKV_DEV_BAD_PAIR, PKV_DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 PKV_DEV_BAD_QUERY_RANGE = 32
+PKV_DECODE_OVERLAP_PREVIOUS = 1
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 BLOCK = 16
 
@@ -73,6 +74,8 @@ def lib():
                                                       vp, vp, c_sz, vp]),
         "pkv_paged_decode_append_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, vp, vp, c_i32, vp, c_i32,
                                                              ctypes.c_float, vp, vp, c_sz, vp]),
+        "pkv_paged_decode_append_attention_ex": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, vp, vp, c_i32, vp, c_i32,
+                                                                ctypes.c_float, vp, vp, c_sz, c_u32, vp]),
         "pkv_paged_decode_attention_static": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32,
                                                              ctypes.c_float, vp, vp]),
         "pkv_paged_prefill_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
@@ -211,8 +214,13 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
 
 
 def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_new, k_pool, v_pool, block_tables,
-                                      context_lens, scale: float, out, workspace=None, stream=None) -> None:
-    """One decode step of one layer: append each sequence's new K/V row at position len-1, then attend."""
+                                      context_lens, scale: float, out, workspace=None, stream=None,
+                                      overlap_previous: bool = False) -> None:
+    """One decode step of one layer: append each sequence's new K/V row at position len-1, then attend.
+
+    overlap_previous: launch with PKV_DECODE_OVERLAP_PREVIOUS (only when the previous kernel on the
+    stream is this call for the previous layer of the same step).
+    """
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
     n_seqs = int(q.shape[0])
@@ -225,13 +233,14 @@ def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_n
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    rc = lib().pkv_paged_decode_append_attention(
+    rc = lib().pkv_paged_decode_append_attention_ex(
         ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape), _dev(k_new, "k_new", dt, kvshape),
         _dev(v_new, "v_new", dt, kvshape), _dev(k_pool, "k_pool", dt, pool_shape(desc)),
         _dev(v_pool, "v_pool", dt, pool_shape(desc)),
         _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
         _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
-        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
+        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes,
+        PKV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0, _stream_handle(stream))
     _check(rc, "pkv_paged_decode_append_attention")
 
 

@@ -171,3 +171,50 @@ def test_chunked_prefill_steps_match_oracle(dtype, n_q, n_kv, d):
     assert cow_seen == 2                       # both forks copied the root's partial tail once
     assert pkv.pkv_get_device_status() == 0
     assert cache.mgr.stats() == mo.stats()
+
+
+@pytest.mark.parametrize("dtype,n_q,n_kv,d", [("f16", 8, 8, 128), ("bf16", 16, 4, 256)])
+def test_layer_overlap_is_bit_identical(dtype, n_q, n_kv, d):
+    """Decode steps whose layer launches overlap (PKV_DECODE_OVERLAP_PREVIOUS: each layer's kernel
+    may start while the previous layer's finishes, all layers sharing one split-K workspace) give
+    outputs and pools bit-identical to the same steps launched one after the other."""
+    L, nb = 4, 600
+    lens = [2500, 1, 700, 1800, 33, 1100]  # split-K and single-partition sequences
+    order = W.free_order(nb, 8)
+    results = []
+    for overlap in (True, False):
+        desc = pkv.make_desc(dtype, L, nb, n_q, n_kv, d)
+        cache = PagedKVCache(desc, free_order=order, init="randn", seed=21)
+        for s, n in enumerate(lens):
+            cache.add_sequence(s, n - 1)
+        batch = DecodeBatch(cache, list(range(len(lens))), max_blocks=200)
+        batch.overlap = overlap
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        dt = pkv.torch_dtype(dtype)
+        q = torch.randn((L, len(lens), n_q, d), device="cuda", generator=g).to(dt)
+        kn = torch.randn((L, len(lens), n_kv, d), device="cuda", generator=g).to(dt)
+        vn = torch.randn((L, len(lens), n_kv, d), device="cuda", generator=g).to(dt)
+        outs = []
+        for _ in range(3):
+            out = torch.empty_like(q)
+            batch.step(q, kn, vn, out, 1.0 / np.sqrt(d))
+            outs.append(out)
+        torch.cuda.synchronize()
+        assert pkv.pkv_get_device_status() == 0
+        results.append((torch.stack(outs), cache.k_pool.clone(), cache.v_pool.clone()))
+    for a, b in zip(results[0], results[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_overlap_flag_validation():
+    desc = pkv.make_desc("f16", 1, 4, 2, 2, 64)
+    L = pkv.lib()
+    import ctypes
+    # unknown flag bits are refused before anything else
+    rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4, None, 0,
+                                                1.0, None, None, 0, 2, None)
+    assert rc == pkv.PKV_ERR_INVALID_ARG
+    rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4, None, 0,
+                                                1.0, None, None, 0, 1, None)
+    assert rc == pkv.PKV_OK  # no sequences: nothing to launch
