@@ -263,6 +263,24 @@ int pkv_paged_prefill_attention(const pkv_cache_desc* desc, int32_t layer, const
                                 int32_t max_query_len, float scale, void* out, void* stream);
 
 /*
+ * pkv_paged_prefill_attention with launch flags. PKV_PREFILL_OVERLAP_PREVIOUS launches the kernel
+ * as a programmatic dependent of the previous kernel on `stream` (fp16 / bf16 storage; no effect
+ * for fp32): it may start while that kernel is finishing and read q, the tables, the lengths,
+ * query_start and layer `layer` of the pools before the previous kernel completes; it writes out
+ * and the status word only after, so the call completes after the previous kernel. Set it only
+ * when the previous kernel on the stream writes none of those inputs -- in a chunked-prefill step
+ * that appends the chunk's rows of every layer before the first attention launch, the attention
+ * launch of the previous layer. Unknown flag bits: PKV_ERR_INVALID_ARG. Results are bit-identical
+ * to pkv_paged_prefill_attention.
+ */
+#define PKV_PREFILL_OVERLAP_PREVIOUS 1u
+int pkv_paged_prefill_attention_ex(const pkv_cache_desc* desc, int32_t layer, const void* q, const void* k_pool,
+                                   const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs,
+                                   int32_t n_tokens, int32_t max_query_len, float scale, void* out, uint32_t flags,
+                                   void* stream);
+
+/*
  * Copy-on-write block copies ("01 - Conceito", paragraph 6): for each pair (src, dst) in
  * pairs (device int32 [n_pairs][2]) copy physical block src onto dst in K and V, all layers.
  * Bit-exact. The dst ids must be distinct and disjoint from the src ids (else the result is

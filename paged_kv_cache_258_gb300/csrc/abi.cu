@@ -249,10 +249,10 @@ int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* d, int32_t layer,
                        context_lens, n_seqs, scale, out, workspace, workspace_bytes, stream);
 }
 
-int pkv_paged_prefill_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
-                                const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs,
-                                int32_t n_tokens, int32_t max_query_len, float scale, void* out, void* stream) {
+static int prefill_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                        const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs, int32_t n_tokens,
+                        int32_t max_query_len, float scale, void* out, void* stream) {
     int rc = pkv_validate_desc(d);
     if (rc != PKV_OK) return rc;
     if (layer < 0 || layer >= d->n_layers || n_seqs < 0 || n_tokens < 0 || max_query_len < 0 ||
@@ -285,11 +285,30 @@ int pkv_paged_prefill_attention(const pkv_cache_desc* d, int32_t layer, const vo
     a.n_tokens = n_tokens;
     a.q_tiles = (max_query_len + per_cta - 1) / per_cta;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.overlap_previous = (flags & PKV_PREFILL_OVERLAP_PREVIOUS) != 0 && d->dtype != PKV_F32;
     if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
     cudaError_t err = pkv::launch_prefill(d->dtype, d->head_dim, group, a, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return PKV_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return PKV_OK;
+}
+
+int pkv_paged_prefill_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                                const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs,
+                                int32_t n_tokens, int32_t max_query_len, float scale, void* out, void* stream) {
+    return prefill_call(0u, d, layer, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens, query_start,
+                        n_seqs, n_tokens, max_query_len, scale, out, stream);
+}
+
+int pkv_paged_prefill_attention_ex(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
+                                   const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start, int32_t n_seqs,
+                                   int32_t n_tokens, int32_t max_query_len, float scale, void* out, uint32_t flags,
+                                   void* stream) {
+    if (flags & ~(uint32_t)PKV_PREFILL_OVERLAP_PREVIOUS) return PKV_ERR_INVALID_ARG;
+    return prefill_call(flags, d, layer, q, k_pool, v_pool, block_tables, max_blocks_per_seq, context_lens,
+                        query_start, n_seqs, n_tokens, max_query_len, scale, out, stream);
 }
 
 int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,

@@ -50,6 +50,7 @@ struct PrefillArgs {
     int n_seqs, n_q, n_kv, num_blocks, max_blocks, n_tokens;
     int q_tiles;            // CTAs along the chunk: ceil(max query length / tokens per CTA)
     float scale_log2;       // scale * log2(e)
+    bool overlap_previous = false;  // launch as a programmatic dependent of the previous kernel
 };
 
 // Query rows (token x head-in-group) one prefill CTA covers; tokens per CTA = rows / group.

@@ -244,6 +244,10 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int CL = Tu::CL;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // A launch that follows this one as a programmatic dependent (the next layer's attention of
+    // the same chunk) may start once every CTA has passed here and fill the SMs this grid's last
+    // wave leaves idle. Without such a launch this is a no-op.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tile = a.q_tiles - 1 - (int)blockIdx.x;  // tiles with the most keys start first
     const int g = blockIdx.y;
     const int s = blockIdx.z;
@@ -658,6 +662,10 @@ __global__ void __launch_bounds__(256, 1)
             const int last = n_tiles - 1;
             if (!mbar_wait_bounded(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u)) ok = false;
         }
+        // launched as a programmatic dependent, this grid computed while the previous kernel was
+        // finishing; the outputs are written only once that kernel has completed (so a chain of
+        // such launches completes in order)
+        grid_dependency_wait();
         if (!ok) {
             if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
         } else {
@@ -714,13 +722,15 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.overlap_previous ? 2 : 1;
     err = cudaLaunchKernelEx(&cfg, kern, b, tk, tv);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();

@@ -286,8 +286,10 @@ class PrefillStep:
                  shared partial tail if there is one); the tables are packed;
       2. H2D:    slots, tables, lengths, query offsets and copy pairs in one copy (pinned,
                  double-buffered as in DecodeBatch);
-      3. device: copy-on-write block copies, then per layer the KV append of the chunk rows and
-                 the paged prefill attention (the chunk attends causally to everything cached).
+      3. device: copy-on-write block copies, then the KV append of the chunk rows and the paged
+                 prefill attention (the chunk attends causally to everything cached) of every
+                 layer: without per-layer callbacks all appends go first and the attention
+                 launches overlap (each may start while the previous layer's finishes).
 
     Capacity is fixed at construction: at most max_tokens chunk tokens and max_seqs sequences
     per step, tables at most max_blocks wide.
@@ -296,6 +298,7 @@ class PrefillStep:
     def __init__(self, cache: PagedKVCache, max_tokens: int, max_seqs: int, max_blocks: int, stream=None):
         import torch
         self.cache = cache
+        self.overlap = True  # see step 3
         self.max_tokens, self.max_seqs, self.max_blocks = int(max_tokens), int(max_seqs), int(max_blocks)
         self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
         T, S, mb = self.max_tokens, self.max_seqs, self.max_blocks
@@ -382,6 +385,18 @@ class PrefillStep:
         slots, tables, lens, qs, pairs = self._dev_views(st["n_seqs"], st["n_tok"])
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, pairs[: st["npairs"]], stream=self.stream)
+        if on_attn is None and self.overlap:
+            # every layer's rows first, then the attention launches back to back: layer l > 0 may
+            # start while layer l-1 finishes (it reads only what the appends above wrote), filling
+            # the SMs the previous launch's last wave leaves idle
+            for layer in range(d.n_layers):
+                pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], slots, c.k_pool, c.v_pool,
+                                  stream=self.stream)
+            for layer in range(d.n_layers):
+                pkv.pkv_paged_prefill_attention(d, layer, q[layer], c.k_pool, c.v_pool, tables, lens, qs,
+                                                st["max_q"], scale, out[layer], stream=self.stream,
+                                                overlap_previous=layer > 0)
+            return
         for layer in range(d.n_layers):
             if on_attn is not None:
                 on_attn(layer, "pre")  # before anything of this layer is launched

@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid", 2: "unsupported", 3: "no_blocks", 4: "bad
 PKV_DEV_BAD_BLOCK_ID, PKV_DEV_BAD_CONTEXT_LEN, PKV_DEV_BAD_SLOT, PKV_DEV_BAD_PAIR, PKV_DEV_WAIT_TIMEOUT = 1, 2, 4, 8, 16
 PKV_DEV_BAD_QUERY_RANGE = 32
 PKV_DECODE_OVERLAP_PREVIOUS = 1
+PKV_PREFILL_OVERLAP_PREVIOUS = 1
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 BLOCK = 16
 
@@ -80,6 +81,8 @@ def lib():
                                                              ctypes.c_float, vp, vp]),
         "pkv_paged_prefill_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
                                                        c_i32, ctypes.c_float, vp, vp]),
+        "pkv_paged_prefill_attention_ex": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
+                                                          c_i32, ctypes.c_float, vp, c_u32, vp]),
         "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
@@ -268,11 +271,14 @@ def pkv_paged_decode_attention_static(desc: CacheDesc, layer: int, q, k_pool, v_
 
 
 def pkv_paged_prefill_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, block_tables, context_lens,
-                                query_start, max_query_len: int, scale: float, out, stream=None) -> None:
+                                query_start, max_query_len: int, scale: float, out, stream=None,
+                                overlap_previous: bool = False) -> None:
     """Causal attention of each sequence's chunk of new tokens over its paged cache (one layer).
 
     q, out [n_tokens, n_q, d]; query_start int32 [n_seqs + 1] (device); max_query_len is the
     largest chunk, known to the caller from its own planning (no device read here).
+    overlap_previous: launch with PKV_PREFILL_OVERLAP_PREVIOUS (only when the previous kernel on the
+    stream is this call for the previous layer and every layer's rows were appended before).
     """
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
@@ -281,13 +287,14 @@ def pkv_paged_prefill_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, 
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
     n_seqs, max_blocks = int(block_tables.shape[0]), int(block_tables.shape[1])
     qshape = (n_tokens, desc.n_q_heads, desc.head_dim)
-    rc = lib().pkv_paged_prefill_attention(
+    rc = lib().pkv_paged_prefill_attention_ex(
         ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
         _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
         _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
         _dev(context_lens, "context_lens", t.int32, (n_seqs,)),
         _dev(query_start, "query_start", t.int32, (n_seqs + 1,)), n_seqs, n_tokens, int(max_query_len),
-        float(scale), _dev(out, "out", dt, qshape), _stream_handle(stream))
+        float(scale), _dev(out, "out", dt, qshape), PKV_PREFILL_OVERLAP_PREVIOUS if overlap_previous else 0,
+        _stream_handle(stream))
     _check(rc, "pkv_paged_prefill_attention")
 
 

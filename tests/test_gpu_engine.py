@@ -218,3 +218,48 @@ def test_overlap_flag_validation():
     rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4, None, 0,
                                                 1.0, None, None, 0, 1, None)
     assert rc == pkv.PKV_OK  # no sequences: nothing to launch
+
+
+@pytest.mark.parametrize("dtype,n_q,n_kv,d", [("bf16", 16, 4, 256), ("f16", 8, 8, 128)])
+def test_prefill_layer_overlap_is_bit_identical(dtype, n_q, n_kv, d):
+    """Chunked-prefill steps whose attention launches overlap (all layers' appends first, then
+    PKV_PREFILL_OVERLAP_PREVIOUS launches) give outputs and pools bit-identical to the per-layer
+    append-then-attend order."""
+    from paged_kv_cache_258_gb300.engine import PrefillStep
+    L, nb, T = 3, 400, 1024
+    prompts = {0: 2100, 1: 700}
+    order = W.free_order(nb, 4)
+    results = []
+    for overlap in (True, False):
+        desc = pkv.make_desc(dtype, L, nb, n_q, n_kv, d)
+        cache = PagedKVCache(desc, free_order=order, init="randn", seed=31)
+        ps = PrefillStep(cache, max_tokens=T, max_seqs=2, max_blocks=160)
+        ps.overlap = overlap
+        g = torch.Generator(device="cuda")
+        g.manual_seed(9)
+        dt = pkv.torch_dtype(dtype)
+        done = {s: 0 for s in prompts}
+        outs = []
+        while any(done[s] < prompts[s] for s in prompts):
+            chunks, budget = [], T
+            for s, n in prompts.items():
+                take = min(n - done[s], budget // 2 if len(prompts) > 1 else budget)
+                if take > 0:
+                    chunks.append((s, take, done[s] == 0))
+                    budget -= take
+            n_tok = sum(c[1] for c in chunks)
+            q = torch.randn((L, n_tok, n_q, d), device="cuda", generator=g).to(dt)
+            kn = torch.randn((L, n_tok, n_kv, d), device="cuda", generator=g).to(dt)
+            vn = torch.randn((L, n_tok, n_kv, d), device="cuda", generator=g).to(dt)
+            out = torch.empty_like(q)
+            ps.step(chunks, q, kn, vn, out, 1.0 / np.sqrt(d))
+            outs.append(out)
+            for s, n, _ in chunks:
+                done[s] += n
+        torch.cuda.synchronize()
+        assert pkv.pkv_get_device_status() == 0
+        results.append((outs, cache.k_pool.clone(), cache.v_pool.clone()))
+    for a, b in zip(results[0][0], results[1][0]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(results[0][1].view(torch.int16), results[1][1].view(torch.int16))
+    assert torch.equal(results[0][2].view(torch.int16), results[1][2].view(torch.int16))
