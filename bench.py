@@ -615,19 +615,25 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
     t1 = torch.cuda.Event(enable_timing=True)
     kv = 0
     npairs = 0
-    from paged_kv_cache_258_gb300.engine import LayerCopyPipeline
-    pipe = LayerCopyPipeline(q.shape[0], stream, device)
-    ups = [[(q[l], hq[l]), (k_new[l], hk[l]), (v_new[l], hv[l])] for l in range(q.shape[0])]
-    downs = [[(hout[l], out[l])] for l in range(q.shape[0])]
+    # step i's inputs go up while step i-1 computes and its outputs come down while step i+1 does
+    # (engine.StepCopyPipeline); the layer launches of a step follow each other directly
+    from paged_kv_cache_258_gb300.engine import StepCopyPipeline
+    pipe = StepCopyPipeline(stream, device, lambda: {"q": torch.empty_like(q), "k": torch.empty_like(k_new),
+                                                     "v": torch.empty_like(v_new), "out": torch.empty_like(out)})
+    host_in = {"q": hq, "k": hk, "v": hv}
     t0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            pipe.upload_all(ups, downs)  # layer l's rows go up while earlier layers compute
-            st = batch.step(q, k_new, v_new, out, scale, on_decode=pipe.hook)
-            pipe.finish()                # the step's outputs are on the host
+        pipe.upload(host_in)
+        for i in range(args.steps):
+            dev = pipe.begin()
+            st = batch.step(dev["q"], dev["k"], dev["v"], dev["out"], scale)
+            pipe.end({"out": hout})
+            if i + 1 < args.steps:
+                pipe.upload(host_in)     # the next step's rows, while this step computes
             kv += batch.kv_bytes_last_step()
             npairs += st["npairs"]
             apply_churn(cache, batch, state)
+        pipe.finish()                    # the last step's outputs are on the host
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()

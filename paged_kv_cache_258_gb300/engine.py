@@ -591,3 +591,69 @@ class LayerCopyPipeline:
         ev = __import__("torch").cuda.Event()
         ev.record(self.d2h)
         self.compute.wait_event(ev)
+
+
+class StepCopyPipeline:
+    """Whole-step host <-> device copies overlapped with other steps' kernels.
+
+    Two device buffer sets alternate between steps: step i's inputs go up (on an upload stream)
+    into one set while step i-1's kernels run on the other, and step i's outputs come down (on a
+    download stream) while step i+1 runs. Nothing is recorded between a step's layer launches, so
+    DecodeBatch can launch them back to back as programmatic dependents. Protocol per step:
+    ``dev = upload(host_inputs)`` (may be issued while the previous step runs), ``begin()``, the
+    step's kernels on ``compute_stream`` using ``dev``, ``end(host_outputs)``; ``finish()`` makes
+    the compute stream wait until the last outputs are on the host.
+    """
+
+    def __init__(self, compute_stream, device, make_set):
+        import torch
+        self.compute = compute_stream
+        self.sets = [make_set(), make_set()]  # dicts of device tensors, inputs and outputs
+        self.h2d = torch.cuda.Stream(device)
+        self.d2h = torch.cuda.Stream(device)
+        self.uploaded = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        self.downloaded = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.next = 0  # the set the next upload fills
+        self.cur = None
+
+    def upload(self, host_inputs: dict) -> dict:
+        """Queue the copies of one step's inputs (name -> pinned host tensor) into the next set."""
+        import torch
+        k = self.next
+        dev = self.sets[k]
+        with torch.cuda.stream(self.h2d):
+            if self.used[k]:
+                self.h2d.wait_event(self.done[k])  # the kernels of two steps ago are done with it
+            for name, host in host_inputs.items():
+                dev[name].copy_(host, non_blocking=True)
+            self.uploaded[k].record(self.h2d)
+        self.next ^= 1
+        return dev
+
+    def begin(self) -> dict:
+        """The compute stream waits for the current set's inputs and for the download of its outputs
+        from two steps ago; returns the set."""
+        k = self.next ^ 1
+        self.cur = k
+        self.compute.wait_event(self.uploaded[k])
+        if self.used[k]:
+            self.compute.wait_event(self.downloaded[k])
+        return self.sets[k]
+
+    def end(self, host_outputs: dict) -> None:
+        """Queue the copies of the step's outputs (name -> pinned host tensor) after its kernels."""
+        import torch
+        k = self.cur
+        self.done[k].record(self.compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.done[k])
+            for name, host in host_outputs.items():
+                host.copy_(self.sets[k][name], non_blocking=True)
+            self.downloaded[k].record(self.d2h)
+        self.used[k] = True
+
+    def finish(self) -> None:
+        if self.cur is not None:
+            self.compute.wait_event(self.downloaded[self.cur])

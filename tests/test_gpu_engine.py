@@ -263,3 +263,55 @@ def test_prefill_layer_overlap_is_bit_identical(dtype, n_q, n_kv, d):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(results[0][1].view(torch.int16), results[1][1].view(torch.int16))
     assert torch.equal(results[0][2].view(torch.int16), results[1][2].view(torch.int16))
+
+
+def test_step_copy_pipeline_matches_direct_steps():
+    """Decode steps fed through engine.StepCopyPipeline (inputs from pinned host memory into two
+    alternating device sets, outputs copied back while the next step runs) return on the host
+    exactly what the same steps return on the device when fed directly."""
+    from paged_kv_cache_258_gb300.engine import StepCopyPipeline
+    dtype, n_q, n_kv, d, L, nb = "f16", 8, 4, 128, 3, 300
+    lens = [900, 40, 1500, 300]
+    dt = pkv.torch_dtype(dtype)
+    g = torch.Generator()
+    g.manual_seed(3)
+    n_steps = 4
+    hq = [torch.randn((L, len(lens), n_q, d), generator=g).to(dt).pin_memory() for _ in range(n_steps)]
+    hk = [torch.randn((L, len(lens), n_kv, d), generator=g).to(dt).pin_memory() for _ in range(n_steps)]
+    hv = [torch.randn((L, len(lens), n_kv, d), generator=g).to(dt).pin_memory() for _ in range(n_steps)]
+    caches = []
+    for _ in range(2):
+        cache = PagedKVCache(pkv.make_desc(dtype, L, nb, n_q, n_kv, d), free_order=W.free_order(nb, 6),
+                             init="randn", seed=12)
+        for s, n in enumerate(lens):
+            cache.add_sequence(s, n - 1)
+        caches.append((cache, DecodeBatch(cache, list(range(len(lens))), max_blocks=120)))
+    # direct
+    cache, batch = caches[0]
+    want = []
+    for i in range(n_steps):
+        out = torch.empty(hq[i].shape, dtype=dt, device="cuda")
+        batch.step(hq[i].cuda(), hk[i].cuda(), hv[i].cuda(), out, 0.09)
+        want.append(out.cpu())
+    # pipelined
+    cache, batch = caches[1]
+    stream = batch.stream
+    pipe = StepCopyPipeline(stream, cache.device, lambda: {"q": torch.empty_like(hq[0], device="cuda"),
+                                                           "k": torch.empty_like(hk[0], device="cuda"),
+                                                           "v": torch.empty_like(hv[0], device="cuda"),
+                                                           "out": torch.empty_like(hq[0], device="cuda")})
+    got = [torch.empty_like(hq[0]).pin_memory() for _ in range(n_steps)]
+    with torch.cuda.stream(stream):
+        pipe.upload({"q": hq[0], "k": hk[0], "v": hv[0]})
+        for i in range(n_steps):
+            dev = pipe.begin()
+            batch.step(dev["q"], dev["k"], dev["v"], dev["out"], 0.09)
+            pipe.end({"out": got[i]})
+            if i + 1 < n_steps:
+                pipe.upload({"q": hq[i + 1], "k": hk[i + 1], "v": hv[i + 1]})
+        pipe.finish()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_status() == 0
+    for a, b in zip(want, got):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(caches[0][0].k_pool.view(torch.int16), caches[1][0].k_pool.view(torch.int16))
