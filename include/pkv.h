@@ -19,11 +19,12 @@
  *                  prefix hits, preemptions.
  *
  * Two halves:
- *   - device calls (kv append, paged decode attention, block copy): asynchronous on the
- *     caller's CUDA stream, no host synchronisation, no allocation; every device pointer is
- *     owned by the caller;
+ *   - device calls (kv append, paged decode attention -- optionally with the step's append
+ *     fused in --, chunked-prefill attention, block copy): asynchronous on the caller's CUDA
+ *     stream, no host synchronisation, no allocation; every device pointer is owned by the
+ *     caller;
  *   - a host block manager (pure C, no CUDA): free list, block tables, reference counts,
- *     prefix sharing, copy-on-write decisions and admission in blocks.
+ *     prefix sharing, copy-on-write decisions, admission in blocks, checkpoint / resume.
  *
  * Memory layout (the pages fix none; this library's reading):
  *   pool (K or V) = [n_layers][num_blocks][n_kv_heads][block_size][head_dim] elements,
