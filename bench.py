@@ -849,8 +849,9 @@ def run_serve_gpu(args) -> dict | None:
                         if n:
                             t_dev[:, :n].copy_(t_host[:, :n], non_blocking=True)
                             h2d[0] += t_dev[:, :n].numel() * 2
+            # without per-kernel events the iteration's launches follow each other as dependents
             ex.run(plan, (dq[:, :nd], dk[:, :nd], dv[:, :nd], d_out[:, :nd]),
-                   (pq[:, :nt], pk[:, :nt], pv[:, :nt], p_out[:, :nt]), scale, on_kernel)
+                   (pq[:, :nt], pk[:, :nt], pv[:, :nt], p_out[:, :nt]), scale, on_kernel if timed_events else None)
             if copies:
                 with torch.cuda.stream(stream):
                     if nd:
@@ -884,12 +885,14 @@ def run_serve_gpu(args) -> dict | None:
     sampler = ClockSampler(gpu_uuid(local))
     sampler.start()
     launches0 = pkv.pkv_launch_count()
-    sched, reqs, steps, wall, evs, dec_bytes, pre_flops, _, _ = one_run(False, True)
+    sched, reqs, steps, wall, _, _, pre_flops, _, _ = one_run(False, False)  # value: no events
     launches = pkv.pkv_launch_count() - launches0
     clocks = sampler.stop()
     torch.cuda.synchronize()
     if pkv.pkv_get_device_status(stream):
         raise RuntimeError("device status flags set during the timed run")
+    # roofline: the same trace again with an event pair around every decode launch
+    _, _, _, _, evs, dec_bytes, _, _, _ = one_run(False, True)
     dec_ms = sum(a.elapsed_time(b) for a, b in evs)
     m = sched.metrics()
     tokens = sum(r.generated for r in reqs if r.state == "done")
@@ -913,8 +916,9 @@ def run_serve_gpu(args) -> dict | None:
                                f"response U{{16..128}}, priority 0); GPT-style 32 layers x 32 heads x 128 fp16, "
                                f"pool {P['num_blocks']} blocks ({P['num_blocks'] * 16} tokens)",
                    "scheduler": f"max {T} tokens per iteration, prefill chunks <= {P['chunk']}, <= {D} running",
-                   "step": "one scheduler iteration (plan on the C manager, one metadata upload, CoW copies, per "
-                           "layer chunk append + prefill attention and fused append + decode attention, sync)",
+                   "step": "one scheduler iteration (plan on the C manager, one metadata upload, CoW copies, the "
+                           "chunk appends of every layer, then per layer prefill attention and fused append + "
+                           "decode attention launched as programmatic dependents, sync)",
                    "l2": "no flush: decode iterations read more KV than L2 holds",
                    "parallelism": f"replicas x{ws} (one trace per rank, no collective)"},
         "wall_s": round(wall_max, 3),

@@ -444,6 +444,7 @@ class StepExecutor:
         self.D, self.T, self.S, self.mb = int(max_decode), int(max_tokens), int(max_chunks), int(max_blocks)
         self.P = int(max_pairs) if max_pairs is not None else self.D + self.S
         self.stream = stream if stream is not None else torch.cuda.current_stream(cache.device)
+        self.overlap = True  # without callbacks, an iteration's launches follow each other as dependents
         D, T, S, mb, P = self.D, self.T, self.S, self.mb, self.P
         o = {}
         off = 0
@@ -514,6 +515,9 @@ class StepExecutor:
         if u["n_pairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self._dev("pairs", 2 * u["n_pairs"], (-1, 2)),
                                 stream=self.stream)
+        if on_kernel is None and self.overlap:
+            self._run_overlapped(u, dec_io, pre_io, scale)
+            return u
         for layer in range(d.n_layers):
             if u["n_pre"]:
                 q, k, v, out = (t[layer] for t in pre_io)
@@ -538,6 +542,36 @@ class StepExecutor:
                 if on_kernel is not None:
                     on_kernel("decode", layer, "end")
         return u
+
+    def _run_overlapped(self, u, dec_io, pre_io, scale: float) -> None:
+        """The iteration's chunk rows of every layer first, then per layer the prefill and the decode
+        launch, each (after the first) a programmatic dependent of the one before: a launch reads
+        only what the appends and copies above wrote (a decode sequence appends into its own last
+        block, which no prefill reads), and touches its outputs and the decode workspace only after
+        the previous launch has completed."""
+        c = self.cache
+        d = c.desc
+        if u["n_pre"]:
+            for layer in range(d.n_layers):
+                _, k, v, _ = (t[layer] for t in pre_io)
+                pkv.pkv_kv_append(d, layer, k, v, self._dev("pre_slots", u["n_tok"], i64=True), c.k_pool, c.v_pool,
+                                  stream=self.stream)
+        first = True
+        for layer in range(d.n_layers):
+            if u["n_pre"]:
+                q, _, _, out = (t[layer] for t in pre_io)
+                pkv.pkv_paged_prefill_attention(
+                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * u["wp"], (-1, u["wp"])),
+                    self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
+                    stream=self.stream, overlap_previous=not first)
+                first = False
+            if u["n_dec"]:
+                q, k, v, out = (t[layer] for t in dec_io)
+                pkv.pkv_paged_decode_append_attention(
+                    d, layer, q, k, v, c.k_pool, c.v_pool,
+                    self._dev("dec_tables", u["n_dec"] * u["wd"], (-1, u["wd"])), self._dev("dec_lens", u["n_dec"]),
+                    scale, out, self.workspace, stream=self.stream, overlap_previous=not first)
+                first = False
 
 
 class LayerCopyPipeline:

@@ -21,8 +21,9 @@ from test_scheduler import MirroredManager, VirtualClock
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("overlap", [True, False])
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
-def test_continuous_batching_matches_oracle(dtype):
+def test_continuous_batching_matches_oracle(dtype, overlap):
     L, n_q, n_kv, d, nb = 2, 4, 2, 64, 90
     rng = np.random.default_rng(123)
     order = W.free_order(nb, 77)
@@ -40,6 +41,7 @@ def test_continuous_batching_matches_oracle(dtype):
                             response=int(rng.integers(2, 40)), arrival=float(rng.integers(0, 20)),
                             priority=i % 2, prefix=pre))
     ex = StepExecutor(cache, max_decode=12, max_tokens=96, max_chunks=16, max_blocks=40)
+    ex.overlap = overlap  # launches chained as programmatic dependents, or one after the other
     hk = np.zeros((L, nb, n_kv, 16, d), NP_STORAGE[dtype])
     hv = np.zeros_like(hk)
     scale = 1.0 / np.sqrt(d)
