@@ -433,6 +433,8 @@ class StepExecutor:
     call has been made on the host). One packed metadata image goes up in one copy; then the
     copy-on-write block copies, and per layer the chunk rows' append + paged prefill attention for
     the prefilling sequences and the fused append + paged decode attention for the decoding ones.
+    Without per-kernel callbacks the chunk appends of every layer go first and the attention
+    launches follow each other as programmatic dependents (see _run_overlapped).
     Capacities (decoders, chunk tokens, chunks, copy pairs per iteration; table width) are fixed
     at construction.
     """
