@@ -94,3 +94,19 @@ def test_manager_create_rejects_non_permutation():
     bad = np.array([0, 1, 1], dtype=np.int32)
     assert not L.pkv_mgr_create(3, 16, bad.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
     assert not L.pkv_mgr_create(0, 16, None)
+
+
+def test_overlap_flags_are_validated_before_anything_runs():
+    """The *_ex calls refuse unknown launch-flag bits before looking at anything else, and accept
+    PKV_*_OVERLAP_PREVIOUS (an empty call launches nothing). No GPU is needed."""
+    import ctypes
+    desc = pkv.make_desc("f16", 1, 4, 2, 2, 64)
+    L = pkv.lib()
+    for flags, want in ((2, pkv.PKV_ERR_INVALID_ARG), (pkv.PKV_DECODE_OVERLAP_PREVIOUS, pkv.PKV_OK)):
+        rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4,
+                                                    None, 0, 1.0, None, None, 0, flags, None)
+        assert rc == want
+    for flags, want in ((6, pkv.PKV_ERR_INVALID_ARG), (pkv.PKV_PREFILL_OVERLAP_PREVIOUS, pkv.PKV_OK)):
+        rc = L.pkv_paged_prefill_attention_ex(ctypes.byref(desc), 0, None, None, None, None, 4, None, None, 0, 0,
+                                              0, 1.0, None, flags, None)
+        assert rc == want

@@ -207,19 +207,6 @@ def test_layer_overlap_is_bit_identical(dtype, n_q, n_kv, d):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_overlap_flag_validation():
-    desc = pkv.make_desc("f16", 1, 4, 2, 2, 64)
-    L = pkv.lib()
-    import ctypes
-    # unknown flag bits are refused before anything else
-    rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4, None, 0,
-                                                1.0, None, None, 0, 2, None)
-    assert rc == pkv.PKV_ERR_INVALID_ARG
-    rc = L.pkv_paged_decode_append_attention_ex(ctypes.byref(desc), 0, None, None, None, None, None, None, 4, None, 0,
-                                                1.0, None, None, 0, 1, None)
-    assert rc == pkv.PKV_OK  # no sequences: nothing to launch
-
-
 @pytest.mark.parametrize("dtype,n_q,n_kv,d", [("bf16", 16, 4, 256), ("f16", 8, 8, 128)])
 def test_prefill_layer_overlap_is_bit_identical(dtype, n_q, n_kv, d):
     """Chunked-prefill steps whose attention launches overlap (all layers' appends first, then
