@@ -182,13 +182,15 @@ int pkv_paged_decode_append_attention(const pkv_cache_desc* desc, int32_t layer,
 /*
  * pkv_paged_decode_append_attention with launch flags. PKV_DECODE_OVERLAP_PREVIOUS launches the
  * kernel as a programmatic dependent of the previous kernel on `stream` (fp16 / bf16 storage; the
- * flag has no effect for fp32): it may start while that kernel is finishing and read q, k_new,
- * v_new, the tables, the lengths and layer `layer` of the pools before the previous kernel
- * completes, and it writes the workspace, out and the status word only after. Set it only when
- * the previous kernel on the stream writes none of those inputs -- in a decode step, the call for
- * the previous layer with the same tables, lengths and workspace (its own out, k_new / v_new rows
- * and pool layer are distinct). Unknown flag bits: PKV_ERR_INVALID_ARG. Results are bit-identical
- * to pkv_paged_decode_append_attention.
+ * flag has no effect for fp32): it may start while that kernel is finishing; before the previous
+ * kernel completes it may read q, k_new, v_new, the tables, the lengths and layer `layer` of the
+ * pools and write the new rows into their slots of layer `layer`; it writes the workspace, out
+ * and the status word only after. Set it only when the previous kernel on the stream writes none
+ * of those inputs and reads none of those new rows' slots -- in a decode step, the call for the
+ * previous layer with the same tables, lengths and workspace (its own out, k_new / v_new rows and
+ * pool layer are distinct), or a prefill attention of the same layer over other sequences (a
+ * decoding sequence appends into its own last block, which no other sequence reads). Unknown flag
+ * bits: PKV_ERR_INVALID_ARG. Results are bit-identical to pkv_paged_decode_append_attention.
  */
 #define PKV_DECODE_OVERLAP_PREVIOUS 1u
 int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* desc, int32_t layer, const void* q,
