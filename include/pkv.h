@@ -273,8 +273,8 @@ int pkv_paged_prefill_attention(const pkv_cache_desc* desc, int32_t layer, const
  * and the status word only after, so the call completes after the previous kernel. Set it only
  * when the previous kernel on the stream writes none of those inputs -- in a chunked-prefill step
  * that appends the chunk's rows of every layer before the first attention launch, the attention
- * launch of the previous layer. Unknown flag bits: PKV_ERR_INVALID_ARG. Results are bit-identical
- * to pkv_paged_prefill_attention.
+ * launch of the previous layer, or the previous layer's decode call over other sequences. Unknown
+ * flag bits: PKV_ERR_INVALID_ARG. Results are bit-identical to pkv_paged_prefill_attention.
  */
 #define PKV_PREFILL_OVERLAP_PREVIOUS 1u
 int pkv_paged_prefill_attention_ex(const pkv_cache_desc* desc, int32_t layer, const void* q, const void* k_pool,
