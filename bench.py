@@ -450,22 +450,13 @@ def run_prefill_gpu(args) -> dict | None:
     scale = 1.0 / float(np.sqrt(d))
     seq = 1
 
-    def one_step(on_attn=None, host=None):
+    def one_step(on_attn=None):
         nonlocal seq
         flops = 0.0
         for i, (c0, n) in enumerate(chunks):
-            hook = on_attn
-            if host is not None:  # per-layer copies of this chunk's rows, overlapped with the kernels
-                pipe, hq, hk, hv, hout = host
-                pipe.upload_all([[(q[l, c0:c0 + n], hq[l, c0:c0 + n]), (k_new[l, c0:c0 + n], hk[l, c0:c0 + n]),
-                                  (v_new[l, c0:c0 + n], hv[l, c0:c0 + n])] for l in range(L)],
-                                [[(hout[l, c0:c0 + n], out[l, c0:c0 + n])] for l in range(L)])
-                hook = pipe.hook
             st = ps.step([(seq, n, i == 0)], q[:, c0:c0 + n], k_new[:, c0:c0 + n], v_new[:, c0:c0 + n],
-                         out[:, c0:c0 + n], scale, hook)
+                         out[:, c0:c0 + n], scale, on_attn)
             flops += PrefillStep.attention_flops(st, n_q, d) * L
-        if host is not None:
-            host[0].finish()  # the prompt's outputs are on the host
         cache.free(seq)       # host only: the next step admits the prompt again
         seq += 1
         return flops
@@ -515,19 +506,59 @@ def run_prefill_gpu(args) -> dict | None:
     attn_ms = sum(a.elapsed_time(b) for a, b in ev)
     achieved = flops / (attn_ms * 1e-3) / 1e12
 
-    # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory, outputs back,
-    # per layer on copy streams overlapped with the kernels (engine.LayerCopyPipeline)
-    from paged_kv_cache_258_gb300.engine import LayerCopyPipeline
+    # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory and its outputs
+    # back, on copy streams beside the kernels. Each chunk has its own rows in the device buffers, so
+    # a prompt's uploads are queued at once: chunk i's rows go up as soon as the previous prompt's
+    # chunk i kernels are done with them, chunk i's kernels wait only for those rows (and for the
+    # previous prompt's chunk i outputs to be down), and its outputs go down once its kernels are
+    # done. Nothing is recorded between a chunk's launches, so the layer launches still overlap.
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k_new, v_new))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    host = (LayerCopyPipeline(L, stream, device), hq, hk, hv, hout)
+    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    prev = {"done": None, "down": None}
+
+    def one_step_e2e():
+        nonlocal seq
+        flops = 0.0
+        up, done, down = [], [], []
+        with torch.cuda.stream(h2d_s):
+            for i, (c0, n) in enumerate(chunks):
+                if prev["done"] is not None:
+                    h2d_s.wait_event(prev["done"][i])  # the previous prompt's chunk i has read these rows
+                for l in range(L):
+                    for dev_t, host_t in ((q, hq), (k_new, hk), (v_new, hv)):
+                        dev_t[l, c0:c0 + n].copy_(host_t[l, c0:c0 + n], non_blocking=True)
+                up.append(torch.cuda.Event())
+                up[-1].record(h2d_s)
+        for i, (c0, n) in enumerate(chunks):
+            stream.wait_event(up[i])
+            if prev["down"] is not None:
+                stream.wait_event(prev["down"][i])  # the previous prompt's chunk i outputs are on the host
+            st = ps.step([(seq, n, i == 0)], q[:, c0:c0 + n], k_new[:, c0:c0 + n], v_new[:, c0:c0 + n],
+                         out[:, c0:c0 + n], scale)
+            flops += PrefillStep.attention_flops(st, n_q, d) * L
+            done.append(torch.cuda.Event())
+            done[-1].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done[-1])
+                for l in range(L):
+                    hout[l, c0:c0 + n].copy_(out[l, c0:c0 + n], non_blocking=True)
+                down.append(torch.cuda.Event())
+                down[-1].record(d2h_s)
+        prev.update(done=done, down=down)
+        cache.free(seq)  # host only: the next step admits the prompt again
+        seq += 1
+        return flops
+
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_s.wait_event(e0)  # no copy starts before the timed region
     e2e_flops = 0.0
     for _ in range(args.steps):
-        e2e_flops += one_step(host=host)
+        e2e_flops += one_step_e2e()
+    stream.wait_event(prev["down"][-1])  # the last prompt's outputs are on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", device)

@@ -293,6 +293,23 @@ int pkv_copy_blocks(const pkv_cache_desc* desc, void* k_pool, void* v_pool, cons
                     int32_t n_pairs, void* stream);
 
 /*
+ * Upload one step's metadata -- the packed block tables, context lengths, slots, query starts
+ * and copy pairs that the host block manager wrote ("La idea de PagedAttention", steps 2 and 5:
+ * the kernel takes the block table as an argument) -- from host to device memory with a kernel
+ * whose threads read the host buffer directly over the host link.
+ *   dst       device memory of the current device, 16-byte aligned, `bytes` long
+ *   src_host  page-locked host memory visible to the device (cudaHostAlloc / cudaMallocHost, or
+ *             registered), 16-byte aligned; the caller keeps it unchanged until the upload has
+ *             run on `stream` (record an event after this call)
+ *   bytes     a multiple of 4, at most 1 GiB; 0 is a no-op
+ * Bit-exact. Unlike a copy-engine copy, the upload does not queue behind bulk host-to-device
+ * copies that other streams have in flight: a step's kernels wait only for their own metadata
+ * while the next step's rows stream in beside them. Pageable, device-invisible or misaligned
+ * memory and a dst on another device return PKV_ERR_INVALID_ARG before anything is launched.
+ */
+int pkv_upload_metadata(void* dst, const void* src_host, size_t bytes, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear this library's device status word on the
  * current device (PKV_DEV_* bits, 0 if every device-side value was in range). For tests
  * and debugging; the only call here that blocks the host.

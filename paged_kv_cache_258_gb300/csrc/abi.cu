@@ -335,6 +335,32 @@ int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const i
     return PKV_OK;
 }
 
+int pkv_upload_metadata(void* dst, const void* src_host, size_t bytes, void* stream) {
+    if (bytes == 0) return PKV_OK;
+    if (!dst || !src_host || bytes % 4 != 0 || !aligned16(dst) || !aligned16(src_host)) return PKV_ERR_INVALID_ARG;
+    if (bytes > ((size_t)1 << 30)) return PKV_ERR_INVALID_ARG;
+    cudaPointerAttributes sa{}, da{};
+    if (cudaPointerGetAttributes(&sa, src_host) != cudaSuccess) {
+        cudaGetLastError();  // an unregistered pointer is an argument error, not a sticky one
+        return PKV_ERR_INVALID_ARG;
+    }
+    if (cudaPointerGetAttributes(&da, dst) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (sa.type != cudaMemoryTypeHost || !sa.devicePointer) return PKV_ERR_INVALID_ARG;
+    if (da.type != cudaMemoryTypeDevice || da.device != dev) return PKV_ERR_INVALID_ARG;
+    // the kernel reads through the device's view of the host buffer (the same address under
+    // unified addressing); it must keep the 16-byte alignment the vector loads need
+    if (!aligned16(sa.devicePointer)) return PKV_ERR_INVALID_ARG;
+    if (pkv::launch_upload_metadata(dst, sa.devicePointer, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
 int pkv_get_device_status(void* stream, uint32_t* flags) {
     if (!flags) return PKV_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;

@@ -115,6 +115,8 @@ cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cu
 cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
+// dst device, src device-visible page-locked host memory; both 16-byte aligned, bytes % 4 == 0.
+cudaError_t launch_upload_metadata(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
 // Tensor-core decode (decode_mma.cuh) serves 16-bit storage when G >= kMmaMinGroup and the pool's
 // rows fit the 32-bit TMA row coordinate; everything else runs the CUDA-core kernel (decode.cuh).

@@ -7,9 +7,11 @@ method needs ("04 - Hacia PagedAttention (vista previa)", "La idea de PagedAtten
 
   1. host:   the block manager reserves one slot per sequence (taking a fresh block or
              copying a shared tail on write) and packs the block tables;
-  2. H2D:    slots, tables, lengths and copy pairs go to the device in one copy (one pinned
+  2. H2D:    slots, tables, lengths and copy pairs go to the device in one upload (one pinned
              image per step, double-buffered on the host and on the device, on an upload stream:
-             step i+1's copy overlaps step i's kernels);
+             step i+1's upload overlaps step i's kernels). The upload is a kernel reading the
+             pinned image (pkv_upload_metadata), not a copy-engine copy, so it never waits
+             behind bulk host-to-device copies of other streams;
   3. device: copy-on-write block copies, then per layer the KV append and the paged decode
              attention -- copies before appends (else a copy would overwrite the new row),
              appends before attention (the new token attends to itself). By default the append
@@ -223,7 +225,7 @@ class DecodeBatch:
         with torch.cuda.stream(self.up_stream):
             if dv["used"]:
                 self.up_stream.wait_event(dv["read"])  # the kernels of two steps ago are done with it
-            dv["meta"][:words].copy_(st["meta"][:words], non_blocking=True)
+            pkv.pkv_upload_metadata(dv["meta"][:words], st["meta"][:words], stream=self.up_stream)
             dv["uploaded"].record(self.up_stream)
             st["done"].record(self.up_stream)
         st["used"] = True
@@ -284,8 +286,8 @@ class PrefillStep:
       1. host:   a sequence's first chunk admits it (pkv_mgr_add_seq: blocks for the chunk
                  only); a later chunk extends it (pkv_mgr_extend, all or nothing, copying a
                  shared partial tail if there is one); the tables are packed;
-      2. H2D:    slots, tables, lengths, query offsets and copy pairs in one copy (pinned,
-                 double-buffered as in DecodeBatch);
+      2. H2D:    slots, tables, lengths, query offsets and copy pairs in one upload (pinned,
+                 double-buffered, through pkv_upload_metadata as in DecodeBatch);
       3. device: copy-on-write block copies, then the KV append of the chunk rows and the paged
                  prefill attention (the chunk attends causally to everything cached) of every
                  layer: without per-layer callbacks all appends go first and the attention
@@ -372,10 +374,8 @@ class PrefillStep:
         return st
 
     def upload(self, st: dict) -> None:
-        import torch
-        with torch.cuda.stream(self.stream):
-            self.d_meta.copy_(st["meta"], non_blocking=True)
-            st["done"].record(self.stream)
+        pkv.pkv_upload_metadata(self.d_meta, st["meta"], stream=self.stream)
+        st["done"].record(self.stream)
         st["used"] = True
 
     def run_device(self, st: dict, q, k_new, v_new, out, scale: float, on_attn=None) -> None:
@@ -430,7 +430,8 @@ class StepExecutor:
     """Runs one continuous-batching iteration planned by scheduler.Scheduler on the device.
 
     The plan arrives complete (slots, tables, lengths, query offsets, copy pairs: every manager
-    call has been made on the host). One packed metadata image goes up in one copy; then the
+    call has been made on the host). One packed metadata image goes up in one upload
+    (pkv_upload_metadata); then the
     copy-on-write block copies, and per layer the chunk rows' append + paged prefill attention for
     the prefilling sequences and the fused append + paged decode attention for the decoding ones.
     Without per-kernel callbacks the chunk appends of every layer go first and the attention
@@ -481,7 +482,6 @@ class StepExecutor:
         return v
 
     def upload(self, plan) -> dict:
-        import torch
         n_dec, n_pre, n_tok, n_pairs = plan.n_dec, len(plan.pre_chunks), plan.n_pre_tokens, len(plan.pairs)
         if n_dec > self.D or n_tok > self.T or n_pre > self.S or n_pairs > self.P:
             raise ValueError("iteration exceeds the executor's capacity")
@@ -501,9 +501,8 @@ class StepExecutor:
         self._host(m, "pre_lens")[:n_pre] = plan.pre_lens
         self._host(m, "pre_qs")[: n_pre + 1] = plan.pre_qs
         self._host(m, "pairs")[: 2 * n_pairs] = plan.pairs.reshape(-1)
-        with torch.cuda.stream(self.stream):
-            self.d_meta.copy_(st["meta"], non_blocking=True)
-            st["done"].record(self.stream)
+        pkv.pkv_upload_metadata(self.d_meta, st["meta"], stream=self.stream)
+        st["done"].record(self.stream)
         st["used"] = True
         return dict(n_dec=n_dec, n_pre=n_pre, n_tok=n_tok, n_pairs=n_pairs, wd=wd, wp=wp,
                     max_q=max([n for _, n in plan.pre_chunks], default=0))

@@ -84,6 +84,7 @@ def lib():
         "pkv_paged_prefill_attention_ex": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
                                                           c_i32, ctypes.c_float, vp, c_u32, vp]),
         "pkv_copy_blocks": (ctypes.c_int, [dp, vp, vp, vp, c_i32, vp]),
+        "pkv_upload_metadata": (ctypes.c_int, [vp, vp, c_sz, vp]),
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
         "pkv_selftest_wait_timeout": (ctypes.c_int, [vp]),
@@ -311,6 +312,20 @@ def pkv_copy_blocks(desc: CacheDesc, k_pool, v_pool, pairs, stream=None) -> None
         ctypes.byref(desc), _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
         _dev(pairs, "pairs", t.int32, (n_pairs, 2)), n_pairs, _stream_handle(stream))
     _check(rc, "pkv_copy_blocks")
+
+
+def pkv_upload_metadata(dst, src, stream=None) -> None:
+    """dst (device) <- src (pinned host), same byte size, through a kernel rather than a copy engine."""
+    if not dst.is_cuda or not dst.is_contiguous():
+        raise ValueError("dst must be a contiguous CUDA tensor")
+    if src.is_cuda or not src.is_contiguous() or not src.is_pinned():
+        raise ValueError("src must be a contiguous pinned host tensor")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must have the same byte size")
+    rc = lib().pkv_upload_metadata(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                   _stream_handle(stream))
+    _check(rc, "pkv_upload_metadata")
 
 
 def pkv_get_device_status(stream=None) -> int:

@@ -131,25 +131,36 @@ int main(void) {
         hkn[i] = to_half(uniform());
         hvn[i] = to_half(uniform());
     }
-    void *dq, *dkn, *dvn, *dtab, *dlens, *dout, *ws = NULL;
+    void *dq, *dkn, *dvn, *dmeta, *dout, *ws = NULL;
     CUDA_OK(cudaMalloc(&dq, sizeof hq));
     CUDA_OK(cudaMalloc(&dkn, sizeof hkn));
     CUDA_OK(cudaMalloc(&dvn, sizeof hvn));
-    CUDA_OK(cudaMalloc(&dtab, sizeof tables));
-    CUDA_OK(cudaMalloc(&dlens, sizeof lens));
+    CUDA_OK(cudaMalloc(&dmeta, sizeof tables + sizeof lens));
     CUDA_OK(cudaMalloc(&dout, sizeof hq));
     CUDA_OK(cudaMemcpy(dq, hq, sizeof hq, cudaMemcpyHostToDevice));
     CUDA_OK(cudaMemcpy(dkn, hkn, sizeof hkn, cudaMemcpyHostToDevice));
     CUDA_OK(cudaMemcpy(dvn, hvn, sizeof hvn, cudaMemcpyHostToDevice));
-    CUDA_OK(cudaMemcpy(dtab, tables, sizeof tables, cudaMemcpyHostToDevice));
-    CUDA_OK(cudaMemcpy(dlens, lens, sizeof lens, cudaMemcpyHostToDevice));
+    /* the step's tables and lengths as one pinned image (27 words: six 16-byte words and a
+     * 4-byte tail), uploaded by pkv_upload_metadata; pageable memory is refused */
+    int32_t* hmeta = NULL;
+    CUDA_OK(cudaMallocHost((void**)&hmeta, sizeof tables + sizeof lens));
+    memcpy(hmeta, tables, sizeof tables);
+    memcpy(hmeta + 3 * 8, lens, sizeof lens);
+    CHECK(pkv_upload_metadata(dmeta, tables, sizeof tables, NULL) == PKV_ERR_INVALID_ARG);
+    CHECK(pkv_upload_metadata(dmeta, hmeta, sizeof tables + sizeof lens, NULL) == PKV_OK);
+    const int32_t* dtab = (const int32_t*)dmeta;
+    const int32_t* dlens = (const int32_t*)dmeta + 3 * 8;
     const size_t ws_bytes = pkv_decode_workspace_bytes(&desc, 3, max_blocks);
     if (ws_bytes) CUDA_OK(cudaMalloc(&ws, ws_bytes));
     const float scale = 1.0f / sqrtf((float)d);
-    CHECK(pkv_paged_decode_append_attention(&desc, layer, dq, dkn, dvn, k_pool, v_pool, (const int32_t*)dtab,
-                                            max_blocks, (const int32_t*)dlens, 3, scale, dout, ws, ws_bytes,
-                                            NULL) == PKV_OK);
+    CHECK(pkv_paged_decode_append_attention(&desc, layer, dq, dkn, dvn, k_pool, v_pool, dtab, max_blocks, dlens, 3,
+                                            scale, dout, ws, ws_bytes, NULL) == PKV_OK);
     CUDA_OK(cudaDeviceSynchronize());
+    {
+        int32_t back[3 * 8 + 3];
+        CUDA_OK(cudaMemcpy(back, dmeta, sizeof back, cudaMemcpyDeviceToHost));
+        CHECK(memcmp(back, hmeta, sizeof back) == 0);
+    }
     uint32_t flags = 1;
     CHECK(pkv_get_device_status(NULL, &flags) == PKV_OK && flags == 0);
     uint16_t hout[3 * 8 * 128];

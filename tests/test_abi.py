@@ -110,3 +110,16 @@ def test_overlap_flags_are_validated_before_anything_runs():
         rc = L.pkv_paged_prefill_attention_ex(ctypes.byref(desc), 0, None, None, None, None, 4, None, None, 0, 0,
                                               0, 1.0, None, flags, None)
         assert rc == want
+
+
+def test_upload_metadata_rejects_bad_arguments_before_any_cuda_call():
+    """Sizes and alignment are checked on the host first; an empty upload is a no-op. No GPU."""
+    L = pkv.lib()
+    null, a, mis = ctypes.c_void_p(0), ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10004)
+    assert L.pkv_upload_metadata(null, null, 0, null) == pkv.PKV_OK
+    assert L.pkv_upload_metadata(null, a, 16, null) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_upload_metadata(a, null, 16, null) == pkv.PKV_ERR_INVALID_ARG
+    assert L.pkv_upload_metadata(a, a, 6, null) == pkv.PKV_ERR_INVALID_ARG      # not whole words
+    assert L.pkv_upload_metadata(mis, a, 16, null) == pkv.PKV_ERR_INVALID_ARG    # dst not 16-byte aligned
+    assert L.pkv_upload_metadata(a, mis, 16, null) == pkv.PKV_ERR_INVALID_ARG    # src not 16-byte aligned
+    assert L.pkv_upload_metadata(a, a, (1 << 30) + 4, null) == pkv.PKV_ERR_INVALID_ARG
