@@ -842,8 +842,14 @@ def run_serve_gpu(args) -> dict | None:
                             (L, T, n_kv, d))]
     d_out = torch.empty((L, D, n_q, d), dtype=dt, device=device)
     p_out = torch.empty((L, T, n_q, d), dtype=dt, device=device)
-    host_in = [t.cpu().pin_memory() for t in dev_in]
-    host_out = [torch.empty(t.shape, dtype=dt).pin_memory() for t in (d_out, p_out)]
+    # e2e buffers: an iteration's n rows of a tensor are one contiguous [L, n, heads, d] image at the
+    # front of a flat buffer, so each tensor goes up (or comes down) in one copy
+    flat_dev = [torch.empty(t.numel(), dtype=dt, device=device) for t in dev_in + [d_out, p_out]]
+    flat_host = [t.reshape(-1).cpu().pin_memory() for t in dev_in]
+    flat_host += [torch.empty(t.numel(), dtype=dt).pin_memory() for t in (d_out, p_out)]
+
+    def rows(flat, like, n):
+        return flat[: like.shape[0] * n * like[0, 0].numel()].view(like.shape[0], n, *like.shape[2:])
     scale = 1.0 / float(np.sqrt(d))
     kv_tok = 2 * n_kv * d * 2
 
@@ -873,24 +879,25 @@ def run_serve_gpu(args) -> dict | None:
 
         def execute(plan):
             nd, nt = plan.n_dec, plan.n_pre_tokens
-            dq, dk, dv, pq, pk, pv = dev_in
+            counts = (nd, nd, nd, nt, nt, nt, nd, nt)
             if copies:
+                ins = [rows(fd, like, n) for fd, like, n in zip(flat_dev, dev_in + [d_out, p_out], counts)]
                 with torch.cuda.stream(stream):
-                    for t_dev, t_host, n in zip(dev_in, host_in, (nd, nd, nd, nt, nt, nt)):
-                        if n:
-                            t_dev[:, :n].copy_(t_host[:, :n], non_blocking=True)
-                            h2d[0] += t_dev[:, :n].numel() * 2
+                    for i in range(6):
+                        if counts[i]:
+                            ins[i].copy_(rows(flat_host[i], dev_in[i], counts[i]), non_blocking=True)
+                            h2d[0] += ins[i].numel() * 2
+            else:
+                ins = [t[:, :n] for t, n in zip(dev_in + [d_out, p_out], counts)]
+            dq, dk, dv, pq, pk, pv, do, po = ins
             # without per-kernel events the iteration's launches follow each other as dependents
-            ex.run(plan, (dq[:, :nd], dk[:, :nd], dv[:, :nd], d_out[:, :nd]),
-                   (pq[:, :nt], pk[:, :nt], pv[:, :nt], p_out[:, :nt]), scale, on_kernel if timed_events else None)
+            ex.run(plan, (dq, dk, dv, do), (pq, pk, pv, po), scale, on_kernel if timed_events else None)
             if copies:
                 with torch.cuda.stream(stream):
-                    if nd:
-                        host_out[0][:, :nd].copy_(d_out[:, :nd], non_blocking=True)
-                        d2h[0] += d_out[:, :nd].numel() * 2
-                    if nt:
-                        host_out[1][:, :nt].copy_(p_out[:, :nt], non_blocking=True)
-                        d2h[0] += p_out[:, :nt].numel() * 2
+                    for j, (o, n) in enumerate(((do, nd), (po, nt))):
+                        if n:
+                            rows(flat_host[6 + j], o, n).copy_(o, non_blocking=True)
+                            d2h[0] += o.numel() * 2
             stream.synchronize()                     # tokens of this iteration exist now
             dec_bytes[0] += int(plan.dec_lens.astype(np.int64).sum()) * kv_tok * L
             for i, (o, n) in enumerate(plan.pre_chunks):
