@@ -9,32 +9,52 @@
 //                  the whole chunk in one copy, landing as [panel][16 rows][128 B] (the V tiles
 //                  of prefill, read by the tensor cores one 16-key block at a time).
 // Encoding goes through the driver entry point cuTensorMapEncodeTiled, found once through the
-// runtime; maps are cached by (address, shape, type, box, device) so steady-state calls do not
-// re-encode.
+// runtime; maps are cached by (address, shape, type, box, device) in a hash table so steady-state
+// calls do not re-encode: a step touches up to 3 maps per layer (K panels, V panels, V blocks), so
+// the table holds every map of several multi-layer caches at once. A map depends only on its key,
+// so an entry stays valid even if its pool is freed and another one reuses the address.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
+#include <cstdint>
 #include <mutex>
+#include <unordered_map>
 
 #include "internal.h"
 
 namespace pkv {
 namespace {
 
-struct MapEntry {
+struct MapKey {
     const void* base;
     long long rows;
     int head_dim;
     int dtype;
     int box;
     int device;
-    unsigned long long stamp;  // 0 = empty slot; else last use (least recently used is replaced)
-    CUtensorMap map;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && head_dim == o.head_dim && dtype == o.dtype && box == o.box &&
+               device == o.device;
+    }
 };
 
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        unsigned long long h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+        h ^= (unsigned long long)k.rows + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
+        h ^= (unsigned long long)((k.head_dim << 12) | (k.dtype << 8) | (k.box << 6) | (k.device & 63)) +
+             (h << 6) + (h >> 2);
+        return (size_t)h;
+    }
+};
+
+// Beyond this many maps the table is emptied and refilled on demand (maps are cheap to re-encode;
+// the bound only keeps a process that creates and drops many pools from growing the table).
+constexpr size_t kMaxMaps = 4096;
+
 std::mutex g_map_mu;
-MapEntry g_maps[64];
-unsigned long long g_clock = 0;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash>* g_maps = nullptr;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
@@ -60,16 +80,13 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    const MapKey key{layer_base, rows, head_dim, dtype, box, dev};
     std::lock_guard<std::mutex> lock(g_map_mu);
-    MapEntry* victim = &g_maps[0];
-    for (MapEntry& e : g_maps) {
-        if (e.stamp && e.base == layer_base && e.rows == rows && e.head_dim == head_dim && e.dtype == dtype &&
-            e.box == box && e.device == dev) {
-            e.stamp = ++g_clock;
-            *out = e.map;
-            return cudaSuccess;
-        }
-        if (e.stamp < victim->stamp) victim = &e;
+    if (!g_maps) g_maps = new std::unordered_map<MapKey, CUtensorMap, MapKeyHash>();  // lives until exit
+    const auto hit = g_maps->find(key);
+    if (hit != g_maps->end()) {
+        *out = hit->second;
+        return cudaSuccess;
     }
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     err = encoder(&encode);
@@ -88,14 +105,8 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    victim->base = layer_base;
-    victim->rows = rows;
-    victim->head_dim = head_dim;
-    victim->dtype = dtype;
-    victim->box = box;
-    victim->device = dev;
-    victim->stamp = ++g_clock;
-    victim->map = map;
+    if (g_maps->size() >= kMaxMaps) g_maps->clear();
+    g_maps->emplace(key, map);
     *out = map;
     return cudaSuccess;
 }

@@ -219,15 +219,13 @@ class DecodeBatch:
         return st
 
     def upload(self, st: dict) -> None:
-        import torch
         words = self._o_pair + 2 * st["npairs"]  # only the pairs this step emitted
         dv = self._dev[st["buf"]]
-        with torch.cuda.stream(self.up_stream):
-            if dv["used"]:
-                self.up_stream.wait_event(dv["read"])  # the kernels of two steps ago are done with it
-            pkv.pkv_upload_metadata(dv["meta"][:words], st["meta"][:words], stream=self.up_stream)
-            dv["uploaded"].record(self.up_stream)
-            st["done"].record(self.up_stream)
+        if dv["used"]:
+            self.up_stream.wait_event(dv["read"])  # the kernels of two steps ago are done with it
+        pkv.upload_metadata_ptr(dv["meta"].data_ptr(), st["meta"].data_ptr(), 4 * words, self.up_stream.cuda_stream)
+        dv["uploaded"].record(self.up_stream)
+        st["done"].record(self.up_stream)
         st["used"] = True
 
     def run_device(self, st: dict, q, k_new, v_new, out, scale: float, on_decode=None) -> None:
@@ -239,6 +237,9 @@ class DecodeBatch:
         self.d_slots, self.d_tables, self.d_lens, self.d_pairs = dv["slots"], dv["tables"], dv["lens"], dv["pairs"]
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self.d_pairs[: st["npairs"]], stream=self.stream)
+        if self.fused:  # the step's tensors checked once; each layer is then one C call
+            launch = pkv.decode_append_launcher(d, q, k_new, v_new, c.k_pool, c.v_pool, self.d_tables, self.d_lens,
+                                                scale, out, self.workspace, stream=self.stream)
         for layer in range(d.n_layers):
             if on_decode is not None:
                 on_decode(layer, "pre")  # before anything of this layer is launched
@@ -248,11 +249,7 @@ class DecodeBatch:
                 # layer l > 0 follows the previous layer's launch directly (no callback in between):
                 # it may start while that one finishes (they share only the tables, lengths and the
                 # workspace, which the kernel touches after the previous launch has completed)
-                pkv.pkv_paged_decode_append_attention(d, layer, q[layer], k_new[layer], v_new[layer], c.k_pool,
-                                                      c.v_pool, self.d_tables, self.d_lens, scale, out[layer],
-                                                      self.workspace, stream=self.stream,
-                                                      overlap_previous=self.overlap and layer > 0
-                                                      and on_decode is None)
+                launch(layer, self.overlap and layer > 0 and on_decode is None)
             else:
                 pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], self.d_slots, c.k_pool, c.v_pool,
                                   stream=self.stream)
@@ -374,7 +371,7 @@ class PrefillStep:
         return st
 
     def upload(self, st: dict) -> None:
-        pkv.pkv_upload_metadata(self.d_meta, st["meta"], stream=self.stream)
+        pkv.upload_metadata_ptr(self.d_meta.data_ptr(), st["meta"].data_ptr(), 4 * self._words, self.stream.cuda_stream)
         st["done"].record(self.stream)
         st["used"] = True
 
@@ -385,26 +382,25 @@ class PrefillStep:
         slots, tables, lens, qs, pairs = self._dev_views(st["n_seqs"], st["n_tok"])
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, pairs[: st["npairs"]], stream=self.stream)
+        append = pkv.append_launcher(d, k_new, v_new, slots, c.k_pool, c.v_pool, stream=self.stream)
+        attend = pkv.prefill_launcher(d, q, c.k_pool, c.v_pool, tables, lens, qs, st["max_q"], scale, out,
+                                      stream=self.stream)
         if on_attn is None and self.overlap:
             # every layer's rows first, then the attention launches back to back: layer l > 0 may
             # start while layer l-1 finishes (it reads only what the appends above wrote), filling
             # the SMs the previous launch's last wave leaves idle
             for layer in range(d.n_layers):
-                pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], slots, c.k_pool, c.v_pool,
-                                  stream=self.stream)
+                append(layer)
             for layer in range(d.n_layers):
-                pkv.pkv_paged_prefill_attention(d, layer, q[layer], c.k_pool, c.v_pool, tables, lens, qs,
-                                                st["max_q"], scale, out[layer], stream=self.stream,
-                                                overlap_previous=layer > 0)
+                attend(layer, layer > 0)
             return
         for layer in range(d.n_layers):
             if on_attn is not None:
                 on_attn(layer, "pre")  # before anything of this layer is launched
-            pkv.pkv_kv_append(d, layer, k_new[layer], v_new[layer], slots, c.k_pool, c.v_pool, stream=self.stream)
+            append(layer)
             if on_attn is not None:
                 on_attn(layer, "start")
-            pkv.pkv_paged_prefill_attention(d, layer, q[layer], c.k_pool, c.v_pool, tables, lens, qs, st["max_q"],
-                                            scale, out[layer], stream=self.stream)
+            attend(layer)
             if on_attn is not None:
                 on_attn(layer, "end")
 
@@ -501,7 +497,8 @@ class StepExecutor:
         self._host(m, "pre_lens")[:n_pre] = plan.pre_lens
         self._host(m, "pre_qs")[: n_pre + 1] = plan.pre_qs
         self._host(m, "pairs")[: 2 * n_pairs] = plan.pairs.reshape(-1)
-        pkv.pkv_upload_metadata(self.d_meta, st["meta"], stream=self.stream)
+        pkv.upload_metadata_ptr(self.d_meta.data_ptr(), st["meta"].data_ptr(),
+                                self.d_meta.numel() * 4, self.stream.cuda_stream)
         st["done"].record(self.stream)
         st["used"] = True
         return dict(n_dec=n_dec, n_pre=n_pre, n_tok=n_tok, n_pairs=n_pairs, wd=wd, wp=wp,
@@ -516,62 +513,63 @@ class StepExecutor:
         if u["n_pairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self._dev("pairs", 2 * u["n_pairs"], (-1, 2)),
                                 stream=self.stream)
+        append, attend, decode = self._launchers(u, dec_io, pre_io, scale)
         if on_kernel is None and self.overlap:
-            self._run_overlapped(u, dec_io, pre_io, scale)
+            self._run_overlapped(u, append, attend, decode)
             return u
         for layer in range(d.n_layers):
             if u["n_pre"]:
-                q, k, v, out = (t[layer] for t in pre_io)
-                pkv.pkv_kv_append(d, layer, k, v, self._dev("pre_slots", u["n_tok"], i64=True), c.k_pool, c.v_pool,
-                                  stream=self.stream)
+                append(layer)
                 if on_kernel is not None:
                     on_kernel("prefill", layer, "start")
-                pkv.pkv_paged_prefill_attention(
-                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * u["wp"], (-1, u["wp"])),
-                    self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
-                    stream=self.stream)
+                attend(layer)
                 if on_kernel is not None:
                     on_kernel("prefill", layer, "end")
             if u["n_dec"]:
-                q, k, v, out = (t[layer] for t in dec_io)
                 if on_kernel is not None:
                     on_kernel("decode", layer, "start")
-                pkv.pkv_paged_decode_append_attention(
-                    d, layer, q, k, v, c.k_pool, c.v_pool,
-                    self._dev("dec_tables", u["n_dec"] * u["wd"], (-1, u["wd"])), self._dev("dec_lens", u["n_dec"]),
-                    scale, out, self.workspace, stream=self.stream)
+                decode(layer)
                 if on_kernel is not None:
                     on_kernel("decode", layer, "end")
         return u
 
-    def _run_overlapped(self, u, dec_io, pre_io, scale: float) -> None:
+    def _launchers(self, u, dec_io, pre_io, scale: float):
+        """The iteration's per-layer launches (None where it has no such work), tensors checked once."""
+        c = self.cache
+        d = c.desc
+        append = attend = decode = None
+        if u["n_pre"]:
+            q, k, v, out = pre_io
+            append = pkv.append_launcher(d, k, v, self._dev("pre_slots", u["n_tok"], i64=True), c.k_pool, c.v_pool,
+                                         stream=self.stream)
+            attend = pkv.prefill_launcher(
+                d, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * u["wp"], (-1, u["wp"])),
+                self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
+                stream=self.stream)
+        if u["n_dec"]:
+            q, k, v, out = dec_io
+            decode = pkv.decode_append_launcher(
+                d, q, k, v, c.k_pool, c.v_pool, self._dev("dec_tables", u["n_dec"] * u["wd"], (-1, u["wd"])),
+                self._dev("dec_lens", u["n_dec"]), scale, out, self.workspace, stream=self.stream)
+        return append, attend, decode
+
+    def _run_overlapped(self, u, append, attend, decode) -> None:
         """The iteration's chunk rows of every layer first, then per layer the prefill and the decode
         launch, each (after the first) a programmatic dependent of the one before: a launch reads
         only what the appends and copies above wrote (a decode sequence appends into its own last
         block, which no prefill reads), and touches its outputs and the decode workspace only after
         the previous launch has completed."""
-        c = self.cache
-        d = c.desc
-        if u["n_pre"]:
-            for layer in range(d.n_layers):
-                _, k, v, _ = (t[layer] for t in pre_io)
-                pkv.pkv_kv_append(d, layer, k, v, self._dev("pre_slots", u["n_tok"], i64=True), c.k_pool, c.v_pool,
-                                  stream=self.stream)
+        n_layers = self.cache.desc.n_layers
+        if append is not None:
+            for layer in range(n_layers):
+                append(layer)
         first = True
-        for layer in range(d.n_layers):
-            if u["n_pre"]:
-                q, _, _, out = (t[layer] for t in pre_io)
-                pkv.pkv_paged_prefill_attention(
-                    d, layer, q, c.k_pool, c.v_pool, self._dev("pre_tables", u["n_pre"] * u["wp"], (-1, u["wp"])),
-                    self._dev("pre_lens", u["n_pre"]), self._dev("pre_qs", u["n_pre"] + 1), u["max_q"], scale, out,
-                    stream=self.stream, overlap_previous=not first)
+        for layer in range(n_layers):
+            if attend is not None:
+                attend(layer, not first)
                 first = False
-            if u["n_dec"]:
-                q, k, v, out = (t[layer] for t in dec_io)
-                pkv.pkv_paged_decode_append_attention(
-                    d, layer, q, k, v, c.k_pool, c.v_pool,
-                    self._dev("dec_tables", u["n_dec"] * u["wd"], (-1, u["wd"])), self._dev("dec_lens", u["n_dec"]),
-                    scale, out, self.workspace, stream=self.stream, overlap_previous=not first)
+            if decode is not None:
+                decode(layer, not first)
                 first = False
 
 

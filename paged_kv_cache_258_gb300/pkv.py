@@ -328,6 +328,112 @@ def pkv_upload_metadata(dst, src, stream=None) -> None:
     _check(rc, "pkv_upload_metadata")
 
 
+def upload_metadata_ptr(dst_ptr: int, src_ptr: int, nbytes: int, stream_handle: int) -> None:
+    """pkv_upload_metadata on raw pointers (the engine keeps its pinned and device images' addresses)."""
+    _check(lib().pkv_upload_metadata(dst_ptr, src_ptr, nbytes, stream_handle), "pkv_upload_metadata")
+
+
+# ---- per-step launchers: a step's tensors validated once, one C call per layer ---------------------
+#
+# A step launches the same call for every layer with the same [L, ...] tensors. The launchers below
+# check them once (device, dtype, shape, each layer's slice contiguous -- views of larger buffers are
+# fine) and keep raw addresses, so a layer's launch is a single call into the C ABI with the same
+# arguments the per-call bindings above would pass.
+
+def _layered(x, name, dtype, n_layers: int, row_shape):
+    """(address of layer 0, bytes between layers) of a [n_layers, *row_shape] tensor."""
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if tuple(x.shape) != (n_layers, *row_shape):
+        raise ValueError(f"{name} must have shape {(n_layers, *row_shape)}, got {tuple(x.shape)}")
+    if not x[0].is_contiguous():
+        raise ValueError(f"{name}: each layer's slice must be contiguous")
+    return x.data_ptr(), x.stride(0) * x.element_size()
+
+
+def _raw_stream(stream) -> int:
+    return _stream_handle(stream).value or 0
+
+
+def decode_append_launcher(desc: CacheDesc, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens,
+                           scale: float, out, workspace=None, stream=None):
+    """launch(layer, overlap_previous=False): pkv_paged_decode_append_attention_ex of one layer, with
+    q/out [L, n, n_q, d] and k_new/v_new [L, n, n_kv, d] validated here once."""
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    L, n = desc.n_layers, int(q.shape[1])
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [n_seqs, max_blocks]")
+    mb = int(block_tables.shape[1])
+    q0, qs = _layered(q, "q", dt, L, (n, desc.n_q_heads, desc.head_dim))
+    o0, os_ = _layered(out, "out", dt, L, (n, desc.n_q_heads, desc.head_dim))
+    k0, ks = _layered(k_new, "k_new", dt, L, (n, desc.n_kv_heads, desc.head_dim))
+    v0, vs = _layered(v_new, "v_new", dt, L, (n, desc.n_kv_heads, desc.head_dim))
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
+    tb = _dev(block_tables, "block_tables", t.int32, (n, mb)).value
+    ln = _dev(context_lens, "context_lens", t.int32, (n,)).value
+    wsp, wsb = (None, 0) if workspace is None else (_dev(workspace, "workspace").value,
+                                                    workspace.numel() * workspace.element_size())
+    fn, dref, sc, sh = lib().pkv_paged_decode_append_attention_ex, ctypes.byref(desc), float(scale), _raw_stream(stream)
+
+    def launch(layer: int, overlap_previous: bool = False) -> None:
+        rc = fn(dref, layer, q0 + layer * qs, k0 + layer * ks, v0 + layer * vs, kp, vp, tb, mb, ln, n, sc,
+                o0 + layer * os_, wsp, wsb, PKV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0, sh)
+        if rc:
+            raise PkvError(rc, "pkv_paged_decode_append_attention")
+    return launch
+
+
+def prefill_launcher(desc: CacheDesc, q, k_pool, v_pool, block_tables, context_lens, query_start,
+                     max_query_len: int, scale: float, out, stream=None):
+    """launch(layer, overlap_previous=False): pkv_paged_prefill_attention_ex of one layer, with
+    q/out [L, n_tokens, n_q, d] validated here once."""
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    L, n_tok = desc.n_layers, int(q.shape[1])
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [n_seqs, max_blocks]")
+    n_seqs, mb = int(block_tables.shape[0]), int(block_tables.shape[1])
+    q0, qs = _layered(q, "q", dt, L, (n_tok, desc.n_q_heads, desc.head_dim))
+    o0, os_ = _layered(out, "out", dt, L, (n_tok, desc.n_q_heads, desc.head_dim))
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
+    tb = _dev(block_tables, "block_tables", t.int32, (n_seqs, mb)).value
+    ln = _dev(context_lens, "context_lens", t.int32, (n_seqs,)).value
+    qsd = _dev(query_start, "query_start", t.int32, (n_seqs + 1,)).value
+    fn, dref, sc, sh = lib().pkv_paged_prefill_attention_ex, ctypes.byref(desc), float(scale), _raw_stream(stream)
+    mq = int(max_query_len)
+
+    def launch(layer: int, overlap_previous: bool = False) -> None:
+        rc = fn(dref, layer, q0 + layer * qs, kp, vp, tb, mb, ln, qsd, n_seqs, n_tok, mq, sc, o0 + layer * os_,
+                PKV_PREFILL_OVERLAP_PREVIOUS if overlap_previous else 0, sh)
+        if rc:
+            raise PkvError(rc, "pkv_paged_prefill_attention")
+    return launch
+
+
+def append_launcher(desc: CacheDesc, k, v, slot_mapping, k_pool, v_pool, stream=None):
+    """launch(layer): pkv_kv_append of one layer, with k/v [L, n_tokens, n_kv, d] validated here once."""
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    L, n_tok = desc.n_layers, int(k.shape[1])
+    k0, ks = _layered(k, "k", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim))
+    v0, vs = _layered(v, "v", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim))
+    sl = _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,)).value
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
+    fn, dref, sh = lib().pkv_kv_append, ctypes.byref(desc), _raw_stream(stream)
+
+    def launch(layer: int) -> None:
+        rc = fn(dref, layer, k0 + layer * ks, v0 + layer * vs, sl, n_tok, kp, vp, sh)
+        if rc:
+            raise PkvError(rc, "pkv_kv_append")
+    return launch
+
+
 def pkv_get_device_status(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pkv_get_device_status(_stream_handle(stream), ctypes.byref(flags)), "pkv_get_device_status")
