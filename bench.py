@@ -1033,37 +1033,56 @@ def run_append_copy_gpu(args) -> dict | None:
     # The 32 appends of a step (~1-2 us of GPU work each) are replayed from a CUDA graph, as a
     # serving loop would issue them: launched one by one from Python they wait on the host. The
     # graph reads the step's slots from a fixed buffer that each step refills on the device.
-    slot_buf = torch.empty(P["batch"], dtype=torch.int64, device=device)
-    slot_buf.copy_(slots[0])
+    # Two sets of (rows, slots, graph): the e2e pass uploads step i+1's rows into one set while
+    # step i's kernels read the other.
+    sets = []
     cap = torch.cuda.Stream()
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):  # one eager pass on the capture stream before capturing
-        for layer in range(L):
-            pkv.pkv_kv_append(desc, layer, k_new[layer], v_new[layer], slot_buf, kp, vp)
-    stream.wait_stream(cap)
-    append_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(append_graph, stream=cap):
-        for layer in range(L):
-            pkv.pkv_kv_append(desc, layer, k_new[layer], v_new[layer], slot_buf, kp, vp)
+    for s_ in range(2):
+        kn, vn = (k_new, v_new) if s_ == 0 else (torch.empty_like(k_new), torch.empty_like(v_new))
+        sb = torch.empty(P["batch"], dtype=torch.int64, device=device)
+        sb.copy_(slots[0])
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):  # one eager pass on the capture stream before capturing
+            for layer in range(L):
+                pkv.pkv_kv_append(desc, layer, kn[layer], vn[layer], sb, kp, vp)
+        stream.wait_stream(cap)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            for layer in range(L):
+                pkv.pkv_kv_append(desc, layer, kn[layer], vn[layer], sb, kp, vp)
+        sets.append(dict(k=kn, v=vn, slots=sb, graph=gr, up=torch.cuda.Event(), free=None))
     torch.cuda.synchronize()
 
     def one_step(i, ev=None, host=None):
-        if host is not None:  # the step's inputs from pinned host memory into the buffers the graph reads
-            hk, hv, hsl, hpr = host
-            k_new.copy_(hk, non_blocking=True)
-            v_new.copy_(hv, non_blocking=True)
-            slot_buf.copy_(hsl[i], non_blocking=True)
-            pairs.copy_(hpr, non_blocking=True)
+        st = sets[i % 2] if host is not None else sets[0]
+        if host is not None:
+            # the step's rows from pinned host memory on the copy stream, into the set the graph of
+            # step i - 2 has finished reading; slots and pairs through the metadata-upload kernel,
+            # which does not wait behind the row copies
+            hk, hv, hsl, hpr, h2d_s = host
+            with torch.cuda.stream(h2d_s):
+                if st["free"] is not None:
+                    h2d_s.wait_event(st["free"])
+                st["k"].copy_(hk, non_blocking=True)
+                st["v"].copy_(hv, non_blocking=True)
+                st["up"].record(h2d_s)
+            pkv.pkv_upload_metadata(st["slots"], hsl[i], stream=stream)
+            pkv.pkv_upload_metadata(pairs, hpr, stream=stream)
         else:
-            slot_buf.copy_(slots[i])
+            st["slots"].copy_(slots[i])
         if ev is not None:
             ev[0].record(stream)
         pkv.pkv_copy_blocks(desc, kp, vp, pairs)  # copies first, then the new rows (step order)
         if ev is not None:
             ev[1].record(stream)
-        append_graph.replay()
+        if host is not None:
+            stream.wait_event(st["up"])
+        st["graph"].replay()
         if ev is not None:
             ev[2].record(stream)
+        if host is not None:
+            st["free"] = torch.cuda.Event()
+            st["free"].record(stream)
 
     for i in range(args.warmup):
         one_step(i)
@@ -1098,13 +1117,14 @@ def run_append_copy_gpu(args) -> dict | None:
     # e2e: new rows, slots and pairs from pinned host memory each step; one destination block of
     # layer 0 read back (the copy's result) at the end of every step
     host = (k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), torch.from_numpy(slots_h).pin_memory(),
-            torch.from_numpy(pairs_h).pin_memory())
+            torch.from_numpy(pairs_h).pin_memory(), torch.cuda.Stream(device))
     back = torch.empty(kp[0, 0].shape, dtype=kp.dtype).pin_memory()
     dst0 = int(pairs_h[0, 1])
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    host[-1].wait_event(e0)  # no copy starts before the timed region
     for j in range(args.steps):
         one_step(args.warmup + 2 * args.steps + j, host=host)
         back.copy_(kp[0, dst0], non_blocking=True)

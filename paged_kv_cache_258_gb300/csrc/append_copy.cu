@@ -5,8 +5,6 @@
 // copy_blocks ("PagedAttention e continuous batching", "01 - Conceito", paragraph 6): a
 // diverging branch gets a private copy of the shared block before it writes into it.
 // Both are pure byte moves with 16-byte vector accesses; they are bit-exact by construction.
-// upload_metadata moves a step's block tables, lengths and slots from page-locked host memory
-// into device memory through the SMs instead of a copy engine.
 #include "common.cuh"
 #include "internal.h"
 
@@ -72,31 +70,6 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a) {
             if (i < n) d[i] = r[u];
         }
     }
-}
-
-// One 16-byte word per thread, read straight from page-locked host memory over the host link
-// (.cv: never served from a cache line fetched before the host rewrote the buffer); a ragged tail
-// of 4-byte words goes to the last threads of the grid.
-__global__ void __launch_bounds__(256) upload_metadata_kernel(uint4* __restrict__ dst,
-                                                              const uint4* __restrict__ src, size_t n16,
-                                                              uint32_t* __restrict__ dst_tail,
-                                                              const uint32_t* __restrict__ src_tail, int n_tail) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n16) dst[i] = __ldcv(src + i);
-    const size_t t = i - n16;
-    if (i >= n16 && t < (size_t)n_tail) dst_tail[t] = __ldcv(src_tail + t);
-}
-
-cudaError_t launch_upload_metadata(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
-    const size_t n16 = bytes / 16;
-    const int n_tail = (int)((bytes % 16) / 4);
-    const size_t threads = n16 + (size_t)n_tail;
-    const unsigned ctas = (unsigned)((threads + 255) / 256);
-    upload_metadata_kernel<<<ctas, 256, 0, stream>>>(
-        static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16,
-        reinterpret_cast<uint32_t*>(static_cast<char*>(dst) + n16 * 16),
-        reinterpret_cast<const uint32_t*>(static_cast<const char*>(src) + n16 * 16), n_tail);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
