@@ -573,59 +573,6 @@ class StepExecutor:
                 first = False
 
 
-class LayerCopyPipeline:
-    """Per-layer host <-> device copies overlapped with the layer kernels.
-
-    A step's inputs and outputs live in pinned host memory; layer l's inputs go up on an upload
-    stream while earlier layers' kernels run, layer l's kernel waits only for them, and its output
-    goes down on a download stream while later layers run. A layer's device buffers are reused by
-    the next step only after this step's kernel of that layer has read them. Use ``hook`` as the
-    ``on_decode`` / ``on_attn`` callback of DecodeBatch.run_device / PrefillStep.run_device, after
-    ``upload_all`` has queued the step's copies.
-    """
-
-    def __init__(self, n_layers: int, compute_stream, device):
-        import torch
-        self.n = int(n_layers)
-        self.compute = compute_stream
-        self.h2d = torch.cuda.Stream(device)
-        self.d2h = torch.cuda.Stream(device)
-        self.up = [torch.cuda.Event() for _ in range(self.n)]
-        self.done = [torch.cuda.Event() for _ in range(self.n)]
-        self.used = [False] * self.n
-        self._down = None
-
-    def upload_all(self, per_layer_pairs, per_layer_down) -> None:
-        """per_layer_pairs[l]: [(device_dst, host_src), ...]; per_layer_down[l]: [(host_dst, device_src)]."""
-        import torch
-        with torch.cuda.stream(self.h2d):
-            for layer in range(self.n):
-                if self.used[layer]:
-                    self.h2d.wait_event(self.done[layer])  # the previous step's kernel has read them
-                for dst, src in per_layer_pairs[layer]:
-                    dst.copy_(src, non_blocking=True)
-                self.up[layer].record(self.h2d)
-        self._down = per_layer_down
-
-    def hook(self, layer: int, when: str) -> None:
-        import torch
-        if when == "pre":
-            self.compute.wait_event(self.up[layer])
-        elif when == "end":
-            self.done[layer].record(self.compute)
-            self.used[layer] = True
-            with torch.cuda.stream(self.d2h):
-                self.d2h.wait_event(self.done[layer])
-                for dst, src in self._down[layer]:
-                    dst.copy_(src, non_blocking=True)
-
-    def finish(self) -> None:
-        """Make the compute stream wait for the step's downloads (the step's result is on the host)."""
-        ev = __import__("torch").cuda.Event()
-        ev.record(self.d2h)
-        self.compute.wait_event(ev)
-
-
 class StepCopyPipeline:
     """Whole-step host <-> device copies overlapped with other steps' kernels.
 
