@@ -136,7 +136,8 @@ class DecodeBatch:
         dev = cache.device
         n, mb = self.n, self.max_blocks
         # One int32 metadata image per step, [slots (int64) | tables | lens | CoW pairs], so the
-        # upload is a single copy; the device copy has fixed addresses across steps.
+        # upload is a single pkv_upload_metadata launch; the device image has fixed addresses across
+        # steps.
         self._o_tab = 2 * n
         self._o_len = self._o_tab + n * mb
         self._o_pair = self._o_len + n
