@@ -553,6 +553,8 @@ def run_prefill_gpu(args) -> dict | None:
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_sampler = ClockSampler(gpu_uuid(local))  # the copies add power: the e2e pass has its own clocks
+    e2e_sampler.start()
     e0.record(stream)
     h2d_s.wait_event(e0)  # no copy starts before the timed region
     e2e_flops = 0.0
@@ -561,6 +563,7 @@ def run_prefill_gpu(args) -> dict | None:
     stream.wait_event(prev["down"][-1])  # the last prompt's outputs are on the host
     e1.record(stream)
     torch.cuda.synchronize()
+    e2e_clocks = e2e_sampler.stop()
     e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", device)
     e2e_flops = reduce_over_ranks(e2e_flops, "sum", device)
     if rank != 0:
@@ -592,7 +595,7 @@ def run_prefill_gpu(args) -> dict | None:
                      "algorithmic_flops_per_launch": int(flops / n_launch)},
         "e2e": {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * elem),
-                "ms_per_step": round(e2e_ms / args.steps, 3)},
+                "ms_per_step": round(e2e_ms / args.steps, 3), "clocks": e2e_clocks},
         "gpu_launches": int(launches),
         "host_manager_us_per_step": round(ps.manager_s / max(1, (args.warmup + 2 * args.steps)) * 1e6, 1),
         "clocks": clocks,
@@ -652,6 +655,8 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
     pipe = StepCopyPipeline(stream, device, lambda: {"q": torch.empty_like(q), "k": torch.empty_like(k_new),
                                                      "v": torch.empty_like(v_new), "out": torch.empty_like(out)})
     host_in = {"q": hq, "k": hk, "v": hv}
+    sampler = ClockSampler(gpu_uuid(device.index))  # the copies add power: the e2e pass has its own clocks
+    sampler.start()
     t0.record(stream)
     with torch.cuda.stream(stream):
         pipe.upload(host_in)
@@ -667,12 +672,13 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
         pipe.finish()                    # the last step's outputs are on the host
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks = sampler.stop()
     barrier()
     ms = reduce_over_ranks(t0.elapsed_time(t1), "max", device)
     kv = reduce_over_ranks(kv, "sum", device)
     return {"value": round(kv / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d + 8 * npairs // max(args.steps, 1)), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": round(ms / args.steps, 4)}
+            "ms_per_step": round(ms / args.steps, 4), "clocks": clocks}
 
 
 DECODE_SOURCES = ("decode.cuh", "decode_mma.cuh", "common.cuh")
