@@ -123,3 +123,21 @@ def test_upload_metadata_rejects_bad_arguments_before_any_cuda_call():
     assert L.pkv_upload_metadata(mis, a, 16, null) == pkv.PKV_ERR_INVALID_ARG    # dst not 16-byte aligned
     assert L.pkv_upload_metadata(a, mis, 16, null) == pkv.PKV_ERR_INVALID_ARG    # src not 16-byte aligned
     assert L.pkv_upload_metadata(a, a, (1 << 30) + 4, null) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_launchers_refuse_host_tensors_before_any_cuda_call():
+    """The per-step launchers check their tensors on the host first: CPU tensors are refused
+    with ValueError before the library is asked to launch anything. No GPU is needed."""
+    import torch
+    desc = pkv.make_desc("f16", 2, 8, 4, 2, 64)
+    q = torch.zeros((2, 3, 4, 64), dtype=torch.float16)
+    k = torch.zeros((2, 3, 2, 64), dtype=torch.float16)
+    pool = torch.zeros(pkv.pool_shape(desc), dtype=torch.float16)
+    tables = torch.zeros((3, 4), dtype=torch.int32)
+    lens = torch.ones(3, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        pkv.decode_append_launcher(desc, q, k, k, pool, pool, tables, lens, 0.1, q)
+    with pytest.raises(ValueError):
+        pkv.prefill_launcher(desc, q, pool, pool, tables, lens, torch.zeros(4, dtype=torch.int32), 1, 0.1, q)
+    with pytest.raises(ValueError):
+        pkv.append_launcher(desc, k, k, torch.zeros(3, dtype=torch.int64), pool, pool)
