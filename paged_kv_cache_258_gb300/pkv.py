@@ -63,7 +63,6 @@ def lib():
     c_i32, c_i64, c_u32, c_u64, c_sz, vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64,
                                             ctypes.c_size_t, ctypes.c_void_p)
     dp = ctypes.POINTER(CacheDesc)
-    i32p, i64p = ctypes.POINTER(c_i32), ctypes.POINTER(c_i64)
     sigs = {
         "pkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pkv_validate_desc": (ctypes.c_int, [dp]),
@@ -88,20 +87,20 @@ def lib():
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
         "pkv_selftest_wait_timeout": (ctypes.c_int, [vp]),
-        "pkv_mgr_create": (vp, [c_i32, c_i32, i32p]),
+        "pkv_mgr_create": (vp, [c_i32, c_i32, vp]),
         "pkv_mgr_clone": (vp, [vp]),
         "pkv_mgr_destroy": (None, [vp]),
-        "pkv_mgr_add_seq": (ctypes.c_int, [vp, c_i64, c_i32, c_i32, i64p]),
+        "pkv_mgr_add_seq": (ctypes.c_int, [vp, c_i64, c_i32, c_i32, vp]),
         "pkv_mgr_fork": (ctypes.c_int, [vp, c_i64, c_i64]),
-        "pkv_mgr_append_slot": (ctypes.c_int, [vp, c_i64, i64p, i32p, i32p]),
-        "pkv_mgr_append_batch": (ctypes.c_int, [vp, i64p, c_i32, i64p, i32p, i32p, i32p]),
-        "pkv_mgr_extend": (ctypes.c_int, [vp, c_i64, c_i32, i64p, i32p, i32p]),
+        "pkv_mgr_append_slot": (ctypes.c_int, [vp, c_i64, vp, vp, vp]),
+        "pkv_mgr_append_batch": (ctypes.c_int, [vp, vp, c_i32, vp, vp, vp, vp]),
+        "pkv_mgr_extend": (ctypes.c_int, [vp, c_i64, c_i32, vp, vp, vp]),
         "pkv_mgr_free_seq": (ctypes.c_int, [vp, c_i64]),
-        "pkv_mgr_block_table": (ctypes.c_int, [vp, c_i64, i32p, c_i32, i32p, i32p]),
-        "pkv_mgr_pack_tables": (ctypes.c_int, [vp, i64p, c_i32, c_i32, i32p, i32p]),
+        "pkv_mgr_block_table": (ctypes.c_int, [vp, c_i64, vp, c_i32, vp, vp]),
+        "pkv_mgr_pack_tables": (ctypes.c_int, [vp, vp, c_i32, c_i32, vp, vp]),
         "pkv_mgr_stats": (ctypes.c_int, [vp, ctypes.POINTER(Stats)]),
         "pkv_mgr_refcount": (c_i32, [vp, c_i32]),
-        "pkv_mgr_free_list": (c_i32, [vp, i32p, c_i32]),
+        "pkv_mgr_free_list": (c_i32, [vp, vp, c_i32]),
         "pkv_mgr_inject_alloc_failure": (ctypes.c_int, [vp, c_i32]),
         "pkv_mgr_save_bytes": (c_sz, [vp]),
         "pkv_mgr_save": (ctypes.c_int, [vp, vp, c_sz, ctypes.POINTER(c_sz)]),
@@ -453,12 +452,15 @@ def alloc_workspace(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, devic
 
 # ---- host block manager -------------------------------------------------------------------------
 
+# The manager's array arguments are declared void* and take the array's address: building a
+# typed ctypes pointer per argument cost more than the manager call itself. The arrays are
+# contiguous int64 / int32 numpy arrays that the caller keeps alive through the call.
 def _i64p(a):
-    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    return a.ctypes.data
 
 
 def _i32p(a):
-    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return a.ctypes.data
 
 
 class BlockManager:

@@ -175,21 +175,21 @@ class Scheduler:
         self.steps += 1
         preempted = []
         pairs = []
-        # 1. decode: one slot per running, fully prefilled request; preempt on append OOM
+        # 1. decode: one slot per running, fully prefilled request; preempt on append OOM. The
+        # manager appends in order and stops at the first request it cannot serve (one C call for
+        # the rest of the batch per attempt).
         dec = [r for r in self.running if r.state == "decode"]
         dec_slots = []
         i = 0
         while i < len(dec):
-            r = dec[i]
-            rc, slot, src, dst = mgr.append_slot(r.seq)
+            rc, slots, new_pairs, n_done = mgr.append_batch([r.seq for r in dec[i:]])
+            dec_slots.extend(slots.tolist())
+            pairs.extend((int(s), int(d)) for s, d in new_pairs)
+            i += n_done
             if rc == pkv.PKV_OK:
-                dec_slots.append(slot)
-                if src >= 0:
-                    pairs.append((src, dst))
-                i += 1
                 continue
             if rc != pkv.PKV_ERR_NO_BLOCKS:
-                raise pkv.PkvError(rc, "append_slot")
+                raise pkv.PkvError(rc, "append_batch")
             victim = self._preempt_victim()
             # a victim that already took this step's slot gives it back with its blocks
             if victim in dec[:i]:

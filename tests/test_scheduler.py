@@ -52,6 +52,23 @@ class MirroredManager:
         self.calls += 1
         return r
 
+    def append_batch(self, sids):
+        """One C call for the batch; the oracle appends the same sequences one at a time, up to and
+        including the first that fails, and must agree on every slot, pair, count and status."""
+        rc, slots, pairs, n_done = self.c.append_batch(sids)
+        want_slots, want_pairs, st = [], [], "ok"
+        for sid in sids:
+            st, slot, src, dst = self.o.append_slot(int(sid))
+            if st != "ok":
+                break
+            want_slots.append(slot)
+            if src >= 0:
+                want_pairs.append([src, dst])
+        assert self._st(rc) == st and n_done == len(want_slots)
+        assert slots.tolist() == want_slots and pairs.tolist() == want_pairs
+        self.calls += 1
+        return rc, slots, pairs, n_done
+
     def fork(self, p, c):
         rc = self.c.fork(p, c)
         assert self._st(rc) == self.o.fork(p, c)
