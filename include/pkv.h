@@ -20,9 +20,9 @@
  *
  * Two halves:
  *   - device calls (kv append, paged decode attention -- optionally with the step's append
- *     fused in --, chunked-prefill attention, block copy): asynchronous on the caller's CUDA
- *     stream, no host synchronisation, no allocation; every device pointer is owned by the
- *     caller;
+ *     fused in --, chunked-prefill attention, block copy, the upload of a step's metadata):
+ *     asynchronous on the caller's CUDA stream, no host synchronisation, no allocation; every
+ *     device pointer is owned by the caller;
  *   - a host block manager (pure C, no CUDA): free list, block tables, reference counts,
  *     prefix sharing, copy-on-write decisions, admission in blocks, checkpoint / resume.
  *
