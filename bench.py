@@ -11,6 +11,12 @@ divided by the step time, with the step's inputs already in HBM; ``e2e`` is the 
 with the per-step inputs (q, new K/V rows for every layer) copied from pinned host memory and
 the outputs copied back inside the timed region.
 
+The default run (--config gpt) measures the GPT-style batch for the line itself, then the
+long-document, ragged and shared-prefix workloads at full size, each under "configs" with its
+own value, per-launch roofline, e2e, clocks and cpu_baseline (--no-sub-configs skips them).
+Every decode line also carries the read-only HBM bandwidth of the GPU ("read_peak": the library's
+streaming-read probe over 4 GiB) and the fractions of it, beside the copy bandwidth.
+
 --config prefill30k prints the chunked-prefill line instead: one 30,000-token prompt of the
 long-document model prefilled in chunks of 2,048 tokens, ``value`` = causal attention TFLOP/s.
 --config appendcopy times the two copy kernels of the path alone: per step one copy_blocks of 200
@@ -249,17 +255,45 @@ def apply_churn(cache, batch, state):
 # ---------------------------------------------------------------------------------------------
 # GPU arm
 
-def run_gpu(args) -> dict | None:
+def measure_read_peak(device, gib: float = 4.0, repeats: int = 10) -> dict:
+    """Read-only HBM bandwidth of this GPU: the library's streaming-read probe over a buffer far
+    larger than L2, timed with CUDA events launch by launch; best and median of the repeats."""
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+    n = int(gib * 2 ** 30) // 4
+    buf = torch.ones(n, dtype=torch.int32, device=device)
+    fold = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        pkv.pkv_hbm_read_probe(buf, fold, stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        pkv.pkv_hbm_read_probe(buf, fold, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    nbytes = n * 4
+    del buf
+    torch.cuda.empty_cache()
+    return {"best_gbs": round(nbytes / (ms[0] * 1e-3) / 1e9, 1),
+            "median_gbs": round(nbytes / (ms[len(ms) // 2] * 1e-3) / 1e9, 1),
+            "bytes": nbytes, "repeats": repeats,
+            "how": f"pkv_hbm_read_probe: one coalesced 16-byte streaming load per word of a {gib:g} GiB buffer, "
+                   f"CUDA events per launch"}
+
+
+def measure_decode(args, config: str, device, rank: int, ws: int, read_peak: dict | None,
+                   cpu: bool, cpu_budget: float) -> dict:
+    """One decode workload at full size on this rank: the value pass (steps alone), the roofline
+    pass (an event pair around every decode launch), the e2e pass, and on rank 0 of one GPU the
+    oracle's cpu baseline. Returns the measurements; the pools are released when it returns."""
     import torch
     from paged_kv_cache_258_gb300 import pkv
 
-    ws, rank = init_dist("nccl")
-    _, _, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    pkv.lib()
     wl, wdesc, cache, batch, (q, k_new, v_new, out), state = setup_gpu_case(
-        args.config, args.warmup, args.steps, device, seed_offset=rank, layers=args.layers,
+        config, args.warmup, args.steps, device, seed_offset=rank, layers=args.layers,
         placement=args.placement)
     stream = batch.stream
     scale = wl.scale
@@ -269,7 +303,7 @@ def run_gpu(args) -> dict | None:
         apply_churn(cache, batch, state)
     flags = pkv.pkv_get_device_status(stream)
     if flags:
-        raise RuntimeError(f"device status flags {flags} during warm-up")
+        raise RuntimeError(f"device status flags {flags} during warm-up ({config})")
 
     # ---- timed region: inputs resident in HBM ----
     L = wl.n_layers
@@ -288,7 +322,7 @@ def run_gpu(args) -> dict | None:
             e[1].record(stream)
             cursor["i"] += 1
 
-    sampler = ClockSampler(gpu_uuid(local))
+    sampler = ClockSampler(gpu_uuid(device.index))
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -324,7 +358,7 @@ def run_gpu(args) -> dict | None:
     total_bytes = reduce_over_ranks(kv_bytes, "sum", device)
     total_seqs = reduce_over_ranks(batch.n * args.steps, "sum", device)
     if pkv.pkv_get_device_status(stream):
-        raise RuntimeError("device status flags set during the timed region")
+        raise RuntimeError(f"device status flags set during the timed region ({config})")
 
     durs = [a.elapsed_time(b) for a, b in ev_pairs]
     achieved_gbs = sum(layer_bytes) / (sum(durs) * 1e-3) / 1e9
@@ -332,26 +366,15 @@ def run_gpu(args) -> dict | None:
     # ---- e2e: per-step inputs from pinned host memory, outputs back to pinned host memory ----
     e2e = run_e2e(args, batch, cache, state, (q, k_new, v_new, out), scale, device)
 
-    if rank != 0:
-        return None
     peaks = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
-    line = {
-        "metric": METRIC,
+    res = {
         "value": round(value, 2),
         "unit": "GB/s",
-        "n_gpus": ws,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": wl.dtype,  # the operands of the QK^T and PV products (fp32 storage runs on CUDA cores)
-        "accumulate": "f32",
-        "data": "synthetic (seeded N(0,1) K/V/q; shapes and length mixes of the pages' workloads)",
         "config": {
             "workload": wdesc,
             "kv_dtype": wl.dtype,
@@ -378,7 +401,7 @@ def run_gpu(args) -> dict | None:
             "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
             "unit": "GB/s",
             "frac": round(achieved_gbs / hbm_peak, 4),
-            "traffic": traffic_per_launch(args.config, sum(layer_bytes) / len(layer_bytes)),
+            "traffic": traffic_per_launch(config, sum(layer_bytes) / len(layer_bytes)),
             "launch_ms_mean": round(sum(durs) / len(durs), 5),
             "algorithmic_bytes_per_launch": int(sum(layer_bytes) / len(layer_bytes)),
         },
@@ -388,8 +411,62 @@ def run_gpu(args) -> dict | None:
         "cow_pairs_timed": int(cow_pairs),
         "clocks": clocks,
     }
-    if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cache, batch, wl, budget_s=args.cpu_budget)
+    if read_peak:
+        rp = read_peak["best_gbs"]
+        res["hbm_frac_of_read_peak"] = round(value / rp, 4)
+        res["roofline"]["read_peak_gbs"] = rp
+        res["roofline"]["frac_of_read_peak"] = round(achieved_gbs / rp, 4)
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline(cache, batch, wl, budget_s=cpu_budget)
+    del cache, batch, q, k_new, v_new, out, state
+    return res
+
+
+# the target workloads measured beside the headline one in the default run (one line, keyed objects)
+SUB_CONFIGS = ("longdoc", "ragged", "prefix")
+
+
+def run_gpu(args) -> dict | None:
+    import gc
+
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pkv.lib()
+    read_peak = measure_read_peak(device)
+    cpu = ws == 1 and not args.no_cpu_baseline
+    res = measure_decode(args, args.config, device, rank, ws, read_peak, cpu, args.cpu_budget)
+    subs = {}
+    if args.config == "gpt" and not args.no_sub_configs and args.layers is None:
+        for name in SUB_CONFIGS:
+            gc.collect()
+            torch.cuda.empty_cache()
+            subs[name] = measure_decode(args, name, device, rank, ws, read_peak, cpu, min(args.cpu_budget, 6.0))
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": res["value"],
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": res["dtype"],
+        "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1) K/V/q; shapes and length mixes of the pages' workloads)",
+    }
+    line.update({k: v for k, v in res.items() if k not in line})
+    line["read_peak"] = read_peak
+    if subs:
+        line["configs"] = subs
     return line
 
 
@@ -1272,6 +1349,8 @@ def main(argv=None):
                     choices=["gpt", "ragged", "longdoc", "prefix", "prefill30k", "serve", "appendcopy"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-configs", action="store_true",
+                    help="gpt only: skip the longdoc / ragged / prefix measurements of the default run")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
     ap.add_argument("--placement", default="shuffled", choices=["shuffled", "contiguous"],
                     help="physical placement of each sequence's blocks (indirection-overhead study)")

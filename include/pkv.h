@@ -36,6 +36,12 @@
  *   k, v     = [n_tokens][n_kv_heads][head_dim] (the new rows to append).
  *   block_tables = int32 [n_seqs][max_blocks_per_seq]; context_lens = int32 [n_seqs].
  *
+ * One GPU per call: the pools, q, out and workspaces of a call live in the memory of the device
+ * current at the call. The library caches per-device facts (the device addresses of its status
+ * word and scratch array, the multiprocessor count, TMA tensor maps) for the life of the process:
+ * calling cudaDeviceReset, or otherwise tearing down a device's primary context, while the library
+ * is loaded is not supported (the cached addresses would then be stale).
+ *
  * Status: every call returns PKV_OK (0) or one PKV_ERR_* code; pkv_status_str names it.
  * Argument errors are caught on the host before anything is launched. Values that live on
  * the device (table entries, context lengths, slots, copy pairs) are range-checked inside
@@ -108,9 +114,26 @@ uint64_t pkv_bytes_per_token(const pkv_cache_desc* desc);
 uint64_t pkv_pool_bytes(const pkv_cache_desc* desc);
 
 /*
- * Scratch bytes pkv_paged_decode_attention needs for n_seqs sequences whose tables have
- * max_blocks_per_seq columns: split-K partial results plus one 8-byte arrival counter per
- * (sequence, KV head); 0 when no split is needed.
+ * Split-K geometry of paged decode attention on a device with sm_count multiprocessors, for
+ * n_seqs sequences whose tables have max_blocks_per_seq columns (an interface helper; the pages
+ * describe no kernel). A long context is cut into partitions of *blocks_per_partition table
+ * entries (64, halved down to 4 while the grid n_seqs * n_kv_heads * *n_partitions would hold
+ * fewer than 4 CTAs per multiprocessor), each computed by its own CTA and merged in the same
+ * launch; *workspace_bytes receives the scratch those partials need (0 when *n_partitions is 1).
+ * The decode calls use exactly this geometry with the current device's multiprocessor count.
+ * Host-only arithmetic: needs no GPU. Output pointers may be NULL. PKV_ERR_INVALID_ARG when a
+ * count is not positive; descriptor errors as pkv_validate_desc.
+ */
+int pkv_decode_split_geometry(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq,
+                              int32_t sm_count, int32_t* blocks_per_partition, int32_t* n_partitions,
+                              size_t* workspace_bytes);
+
+/*
+ * Scratch bytes pkv_paged_decode_attention needs on the current device for n_seqs sequences whose
+ * tables have max_blocks_per_seq columns: split-K partial results plus one 8-byte arrival counter
+ * per (sequence, KV head); 0 when no split is needed -- and also when the descriptor or a count is
+ * invalid or no CUDA device can be queried. Equals pkv_decode_split_geometry's *workspace_bytes
+ * for the current device's multiprocessor count (read once per device and cached).
  */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq);
 
@@ -199,6 +222,32 @@ int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* desc, int32_t lay
                                          const int32_t* context_lens, int32_t n_seqs, float scale, void* out,
                                          void* workspace, size_t workspace_bytes, uint32_t flags, void* stream);
 
+/*
+ * Decode attention over a dense, contiguous KV cache: the pre-allocated (batch, heads, maximum
+ * length, head_dim) cache that "04 - Hacia PagedAttention (vista previa)" starts from ("Lo que
+ * funciona en la Fase 22"), read by the same kernels as pkv_paged_decode_attention with the block
+ * table replaced by the identity walk (logical block i of a sequence is its i-th 16-row chunk).
+ * It exists to price the table walk: paging changes where rows live, not the result ("Lo que
+ * deberias llevarte de la Fase 22 sobre la Fase 27", item 2), at the cost of a constant factor
+ * (items 2-3). For query head h and KV head g = h / G:
+ *   out[s][h] = sum_j softmax_j(scale * q[s][h] . K[s][g][j]) V[s][g][j],  j < context_lens[s].
+ *   k_cache, v_cache device [n_layers][n_seqs][n_kv_heads][max_seq_len][head_dim] of desc->dtype,
+ *                 16-byte aligned (desc->num_blocks is not used)
+ *   max_seq_len   positions reserved per sequence: a positive multiple of 16
+ *   context_lens  device int32 [n_seqs], 0 <= len <= max_seq_len (larger: clamped, and
+ *                 PKV_DEV_BAD_CONTEXT_LEN is set)
+ *   q, out, scale as pkv_paged_decode_attention
+ *   workspace     as pkv_paged_decode_attention with max_blocks_per_seq = max_seq_len / 16
+ *   flags         0 or PKV_DECODE_OVERLAP_PREVIOUS (as pkv_paged_decode_append_attention_ex)
+ * Equal, bit for bit, to pkv_paged_decode_attention over a pool holding the same rows in the same
+ * logical order. Rows past context_lens[s] are never used. PKV_ERR_UNSUPPORTED when
+ * n_seqs * n_kv_heads * max_seq_len reaches 2^31 rows.
+ */
+int pkv_dense_decode_attention(const pkv_cache_desc* desc, int32_t layer, const void* q, const void* k_cache,
+                               const void* v_cache, int32_t max_seq_len, const int32_t* context_lens,
+                               int32_t n_seqs, float scale, void* out, void* workspace, size_t workspace_bytes,
+                               uint32_t flags, void* stream);
+
 /* Size of the fixed scratch array used by pkv_paged_decode_attention_static (16 MiB). */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -257,7 +306,11 @@ int pkv_paged_decode_attention_static(const pkv_cache_desc* desc, int32_t layer,
  * PKV_DEV_BAD_QUERY_RANGE. A table entry outside [0, num_blocks) is skipped (its keys count as
  * masked) and sets PKV_DEV_BAD_BLOCK_ID. Rows past a query's position or past the context are
  * never used: NaN there cannot reach the output. No workspace; nothing is allocated.
- * fp16 / bf16 run on the tensor cores; fp32 on the CUDA cores (the precision mode).
+ * fp16 / bf16 run on the tensor cores; fp32 on the CUDA cores (the precision mode). For one GPU:
+ * k_pool and v_pool must be device memory of the current device, because the tensor copies read
+ * them directly; the first fp16 / bf16 call on a pool layer checks this before building its copy
+ * descriptors (cached afterwards by address) and returns PKV_ERR_INVALID_ARG for host memory or
+ * another GPU's memory, launching nothing. The same holds for the fp16 / bf16 decode calls.
  */
 int pkv_paged_prefill_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
                                 const void* k_pool, const void* v_pool, const int32_t* block_tables,
@@ -315,6 +368,19 @@ int pkv_upload_metadata(void* dst, const void* src_host, size_t bytes, void* str
  * and debugging; the only call here that blocks the host.
  */
 int pkv_get_device_status(void* stream, uint32_t* flags);
+
+/*
+ * Measurement helper (the pages have no counterpart): read every byte of buf once, as a plain
+ * coalesced stream, and XOR-fold its 32-bit words into *fold. Timing this call over a buffer much
+ * larger than the L2 cache gives the read-only HBM bandwidth of the device, the ceiling of a kernel
+ * that only reads (paged decode attention writes a few bytes per kilobyte it reads).
+ *   buf    device, 16-byte aligned, `bytes` long (a multiple of 16)
+ *   fold   device uint32, 4-byte aligned; XORed with the fold of buf's words (set it to 0 first to
+ *          read the fold itself: the XOR of every little-endian 32-bit word of buf)
+ * Asynchronous on `stream`. PKV_ERR_INVALID_ARG for a misaligned or NULL pointer or a size that is
+ * not a multiple of 16; bytes == 0 is a no-op.
+ */
+int pkv_hbm_read_probe(const void* buf, size_t bytes, uint32_t* fold, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t pkv_launch_count(void);

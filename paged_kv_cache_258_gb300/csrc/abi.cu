@@ -48,9 +48,9 @@ size_t layer_elems(const pkv_cache_desc* d) {
     return (size_t)d->num_blocks * d->n_kv_heads * d->block_size * d->head_dim;
 }
 
-size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int* bpp_out, int* n_parts_out,
-                        size_t* off_ml = nullptr, size_t* off_cnt = nullptr) {
-    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks);
+size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int sm_count, int* bpp_out,
+                        int* n_parts_out, size_t* off_ml = nullptr, size_t* off_cnt = nullptr) {
+    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks, sm_count);
     const int n_parts = pkv::decode_partitions(max_blocks, bpp);
     if (bpp_out) *bpp_out = bpp;
     if (n_parts_out) *n_parts_out = n_parts;
@@ -62,19 +62,40 @@ size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int
     return bytes;
 }
 
+std::mutex g_sm_mu;
+int g_sm_count[64] = {};
+
 }  // namespace
 
 namespace pkv {
 
 // Blocks per partition: 64 (1,024 tokens) unless the grid would then hold fewer than ~4 CTAs per
-// SM of a GB300 (152 SMs), in which case partitions shrink (down to 4 blocks) to spread one
-// long sequence over more SMs. Depends only on the arguments, so the workspace query and the
-// launch agree on every device.
-int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks) {
-    const long long target = 4LL * 152;
+// SM, in which case partitions shrink (down to 4 blocks) to spread one long sequence over more
+// SMs. Depends only on the arguments, so the workspace query and the launch agree as long as both
+// pass the same SM count (both take it from current_sm_count).
+int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count) {
+    const long long target = 4LL * (sm_count > 0 ? sm_count : 1);
     int bpp = kMaxBpp;
     while (bpp > 4 && (long long)n_seqs * n_kv * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
     return bpp;
+}
+
+// SMs of the current device (cudaDevAttrMultiProcessorCount), read once per device.
+cudaError_t current_sm_count(int* out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sm_mu);
+    if (g_sm_count[dev] <= 0) {
+        int n = 0;
+        err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        if (n <= 0) return cudaErrorInvalidValue;
+        g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return cudaSuccess;
 }
 
 cudaError_t device_status_word(unsigned int** out) { return status_word(out); }
@@ -140,9 +161,28 @@ uint64_t pkv_pool_bytes(const pkv_cache_desc* d) {
     return (uint64_t)d->n_layers * layer_elems(d) * elem_bytes(d->dtype);
 }
 
+int pkv_decode_split_geometry(const pkv_cache_desc* d, int32_t n_seqs, int32_t max_blocks_per_seq,
+                              int32_t sm_count, int32_t* blocks_per_partition, int32_t* n_partitions,
+                              size_t* workspace_bytes) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (n_seqs <= 0 || max_blocks_per_seq <= 0 || sm_count <= 0) return PKV_ERR_INVALID_ARG;
+    int bpp = 0, n_parts = 0;
+    const size_t bytes = decode_workspace(d, n_seqs, max_blocks_per_seq, sm_count, &bpp, &n_parts);
+    if (blocks_per_partition) *blocks_per_partition = bpp;
+    if (n_partitions) *n_partitions = n_parts;
+    if (workspace_bytes) *workspace_bytes = bytes;
+    return PKV_OK;
+}
+
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* d, int32_t n_seqs, int32_t max_blocks_per_seq) {
     if (pkv_validate_desc(d) != PKV_OK || n_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
-    return decode_workspace(d, n_seqs, max_blocks_per_seq, nullptr, nullptr);
+    int sms = 0;
+    if (pkv::current_sm_count(&sms) != cudaSuccess) {
+        cudaGetLastError();  // no usable device: report nothing rather than a guess
+        return 0;
+    }
+    return decode_workspace(d, n_seqs, max_blocks_per_seq, sms, nullptr, nullptr);
 }
 
 int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const void* v, const int64_t* slot_mapping,
@@ -170,32 +210,43 @@ int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const v
     return PKV_OK;
 }
 
-// Shared body of the two decode entry points; k_new / v_new are null unless the append is fused.
+// Shared body of the decode entry points; k_new / v_new are null unless the append is fused. With
+// `dense`, k_pool / v_pool are dense caches [n_layers][n_seqs][n_kv][max_blocks*16][D] walked by
+// identity (block_tables unused) instead of paged pools.
 static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_new,
                        const void* v_new,
                        const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t max_blocks_per_seq,
                        const int32_t* context_lens, int32_t n_seqs, float scale, void* out, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, bool dense = false) {
     int rc = pkv_validate_desc(d);
     if (rc != PKV_OK) return rc;
     if (layer < 0 || layer >= d->n_layers || n_seqs < 0) return PKV_ERR_INVALID_ARG;
     if (n_seqs == 0) return PKV_OK;
     if (max_blocks_per_seq <= 0 || max_blocks_per_seq > (1 << 24)) return PKV_ERR_INVALID_ARG;
     if (n_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (dense && (long long)n_seqs * max_blocks_per_seq >= (1LL << 31) / (long long)(d->n_kv_heads * d->block_size))
+        return PKV_ERR_UNSUPPORTED;  // chunk and row indices of the dense cache are 32-bit
+    if (!q || !k_pool || !v_pool || (!block_tables && !dense) || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
     if ((k_new || v_new) && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    if (pkv::current_sm_count(&sms) != cudaSuccess) return PKV_ERR_CUDA;
     int bpp = 0, n_parts = 0;
     size_t off_ml = 0, off_cnt = 0;
-    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, &bpp, &n_parts, &off_ml, &off_cnt);
+    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, sms, &bpp, &n_parts, &off_ml, &off_cnt);
     if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
 
     pkv::DecodeArgs a;
-    const size_t layer_bytes = layer_elems(d) * elem_bytes(d->dtype);
+    // a dense layer holds n_seqs * max_blocks 16-row chunks per KV head: the pool geometry with
+    // num_blocks = n_seqs * max_blocks
+    const int num_blocks = dense ? n_seqs * max_blocks_per_seq : d->num_blocks;
+    const size_t layer_bytes =
+        (size_t)num_blocks * d->n_kv_heads * d->block_size * d->head_dim * elem_bytes(d->dtype);
     a.q = q;
     a.k_layer = static_cast<const char*>(k_pool) + (size_t)layer * layer_bytes;
     a.v_layer = static_cast<const char*>(v_pool) + (size_t)layer * layer_bytes;
-    a.tables = block_tables;
+    a.tables = dense ? nullptr : block_tables;
+    a.dense = dense;
     a.lens = context_lens;
     a.out = out;
     a.part_o = need ? static_cast<float*>(workspace) : nullptr;
@@ -207,7 +258,7 @@ static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, c
     a.n_seqs = n_seqs;
     a.n_q = d->n_q_heads;
     a.n_kv = d->n_kv_heads;
-    a.num_blocks = d->num_blocks;
+    a.num_blocks = num_blocks;
     a.max_blocks = max_blocks_per_seq;
     a.n_parts = n_parts;
     a.bpp = bpp;
@@ -218,7 +269,7 @@ static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, c
     cudaError_t err = pkv::launch_decode(d->dtype, d->head_dim, d->n_q_heads / d->n_kv_heads, a,
                                          static_cast<cudaStream_t>(stream), &launches);
     g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
-    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return pkv::launch_status(err);
 }
 
 int pkv_paged_decode_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
@@ -247,6 +298,16 @@ int pkv_paged_decode_append_attention_ex(const pkv_cache_desc* d, int32_t layer,
     if (n_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
     return decode_call(flags, d, layer, q, k_new, v_new, k_pool, v_pool, block_tables, max_blocks_per_seq,
                        context_lens, n_seqs, scale, out, workspace, workspace_bytes, stream);
+}
+
+int pkv_dense_decode_attention(const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_cache,
+                               const void* v_cache, int32_t max_seq_len, const int32_t* context_lens, int32_t n_seqs,
+                               float scale, void* out, void* workspace, size_t workspace_bytes, uint32_t flags,
+                               void* stream) {
+    if (flags & ~(uint32_t)PKV_DECODE_OVERLAP_PREVIOUS) return PKV_ERR_INVALID_ARG;
+    if (!d || max_seq_len <= 0 || max_seq_len % pkv::kBlock != 0) return PKV_ERR_INVALID_ARG;
+    return decode_call(flags, d, layer, q, nullptr, nullptr, k_cache, v_cache, nullptr, max_seq_len / pkv::kBlock,
+                       context_lens, n_seqs, scale, out, workspace, workspace_bytes, stream, true);
 }
 
 static int prefill_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, const void* q, const void* k_pool,
@@ -288,7 +349,7 @@ static int prefill_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, 
     a.overlap_previous = (flags & PKV_PREFILL_OVERLAP_PREVIOUS) != 0 && d->dtype != PKV_F32;
     if (status_word(&a.status) != cudaSuccess) return PKV_ERR_CUDA;
     cudaError_t err = pkv::launch_prefill(d->dtype, d->head_dim, group, a, static_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return PKV_ERR_CUDA;
+    if (err != cudaSuccess) return pkv::launch_status(err);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return PKV_OK;
 }

@@ -60,6 +60,17 @@ struct DecodeTuning {
     static constexpr int ST = NW * 2 * STAGE_BYTES > 200 * 1024 ? 1 : (ST_RAW < 2 ? 2 : (ST_RAW > 4 ? 4 : ST_RAW));
 };
 
+// The walk of step a1: the physical block holding logical block `blk` of sequence s (the table entry;
+// a dense cache's identity walk returns blk itself) ...
+__device__ __forceinline__ int walk_entry(const DecodeArgs& a, int s, int blk) {
+    return a.dense ? blk : a.tables[(size_t)s * a.max_blocks + blk];
+}
+// ... and the index of its 16-row chunk of KV head g in the layer seen as [chunks][16][D]: a paged
+// pool stores [block][head], a dense cache [sequence][head][block].
+__device__ __forceinline__ long long chunk_index(const DecodeArgs& a, int s, int g, int phys) {
+    return a.dense ? ((long long)s * a.n_kv + g) * a.max_blocks + phys : (long long)phys * a.n_kv + g;
+}
+
 constexpr int kMergeChunk = 32;  // partitions whose weights are staged in shared memory at a time
 
 // Shared-memory floats the split-K merge needs (flag, row maxima, row sums, one chunk of weights).
@@ -189,11 +200,11 @@ __device__ __forceinline__ void splitk_merge_if_last(const DecodeArgs& a, int s,
 template <typename T, int D, int NT>
 __device__ __forceinline__ void fused_append(const DecodeArgs& a, int s, int g, int p, int ctx, int nb) {
     if (a.k_new == nullptr || p != (nb - 1) / a.bpp) return;
-    const int phys = a.tables[(size_t)s * a.max_blocks + nb - 1];
+    const int phys = walk_entry(a, s, nb - 1);
     if ((unsigned)phys >= (unsigned)a.num_blocks) return;
     constexpr int NCH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
     const size_t src_row = ((size_t)s * a.n_kv + g) * D;
-    const size_t dst_row = (((size_t)phys * a.n_kv + g) * kBlock + (ctx - 1) % kBlock) * D;
+    const size_t dst_row = ((size_t)chunk_index(a, s, g, phys) * kBlock + (ctx - 1) % kBlock) * D;
     for (int i = threadIdx.x; i < 2 * NCH; i += NT) {
         const bool is_v = i >= NCH;
         const int c = is_v ? i - NCH : i;
@@ -260,7 +271,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
     float* s_z = s_zall + warp * G * kBlock;
     float* s_p = s_pall + warp * G * kBlock;
 
-    const int32_t* trow = a.tables + (size_t)s * a.max_blocks + b0;
     static_assert(kMaxBpp % NW == 0, "each warp stages kMaxBpp / NW table entries");
     int* wtab = reinterpret_cast<int*>(smem + S::TAB) + warp * (kMaxBpp / NW);
     const T* kbase = reinterpret_cast<const T*>(a.k_layer);
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
         const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
         wphys[st] = ok ? phys : -1;
         if (ok) {
-            const size_t off = ((size_t)phys * a.n_kv + g) * CHUNK;
+            const size_t off = (size_t)chunk_index(a, s, g, phys) * CHUNK;
             T* dst = wstage + (size_t)st * 2 * CHUNK;
             mbar_arrive_expect_tx(&wbars[st], 2 * CHUNK_BYTES);
             bulk_copy_g2s(dst, kbase + off, CHUNK_BYTES, &wbars[st], policy);
@@ -287,7 +297,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
     };
     // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
     // waits on a global read of the table
-    for (int k = lane; k < nk; k += 32) wtab[k] = trow[warp + k * NW];
+    for (int k = lane; k < nk; k += 32) wtab[k] = walk_entry(a, s, b0 + warp + k * NW);
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < ST && k < nk; ++k) issue(k);

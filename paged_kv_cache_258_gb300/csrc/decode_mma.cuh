@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     int tab_pre = -1;
     {
         const int idx = p * a.bpp + warp + lane * NW;
-        if (lane < kMaxBpp / NW && idx < a.max_blocks) tab_pre = a.tables[(size_t)s * a.max_blocks + idx];
+        if (lane < kMaxBpp / NW && idx < a.max_blocks) tab_pre = walk_entry(a, s, idx);
     }
     int ctx = a.lens[s];
     const int cap = a.max_blocks * kBlock;
@@ -189,7 +189,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     int* wphys = s_phys + warp * ST;
     const uint32_t wstage = smem_addr(smem) + (uint32_t)(warp * ST) * 2 * TILE;
     unsigned char* wstage_ptr = smem + (size_t)warp * ST * 2 * TILE;
-    const int32_t* trow = a.tables + (size_t)s * a.max_blocks + b0;
     static_assert(kMaxBpp % NW == 0, "each warp stages kMaxBpp / NW table entries");
     int* wtab = reinterpret_cast<int*>(smem + S::TAB) + warp * (kMaxBpp / NW);
     const int nk = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
         uint64_t* bar = &wbars[st * 2 + v];
         if (v == 0) wphys[st] = ok ? phys : -1;
         if (ok) {
-            const int row0 = (phys * a.n_kv + g) * kBlock;
+            const int row0 = (int)(chunk_index(a, s, g, phys) * kBlock);
             const uint32_t dst = wstage + (uint32_t)st * 2 * TILE + (uint32_t)v * TILE;
             mbar_arrive_expect_tx(bar, TILE);
 #pragma unroll
@@ -220,7 +219,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
     // waits on a global read of the table
     if (lane < nk) wtab[lane] = tab_pre;
-    (void)trow;
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < ST && k < nk; ++k) {

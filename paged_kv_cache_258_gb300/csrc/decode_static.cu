@@ -63,7 +63,9 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
 
     // Same partition geometry, hence the same scratch need, as pkv_paged_decode_attention.
-    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks_per_seq);
+    int sms = 0;
+    if (pkv::current_sm_count(&sms) != cudaSuccess) return PKV_ERR_CUDA;
+    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks_per_seq, sms);
     const int n_parts = pkv::decode_partitions(max_blocks_per_seq, bpp);
     size_t off_ml = 0, off_cnt = 0;
     const size_t need =
@@ -102,5 +104,5 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     cudaError_t err = pkv::launch_decode(d->dtype, d->head_dim, d->n_q_heads / d->n_kv_heads, a,
                                          static_cast<cudaStream_t>(stream), &launches);
     pkv::count_launches((uint64_t)launches);
-    return err == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return pkv::launch_status(err);
 }

@@ -34,6 +34,10 @@ struct DecodeArgs {
     int bpp;                // blocks per partition
     float scale_log2;       // scale * log2(e): logits are kept in base 2
     bool overlap_previous = false;  // launch as a programmatic dependent of the previous kernel
+    // Dense cache instead of a paged pool: k_layer / v_layer are [n_seqs][n_kv][max_blocks*16][D],
+    // logical block i of sequence s is chunk (s*n_kv + g)*max_blocks + i (the identity walk, no
+    // table); tables is unused and num_blocks = n_seqs * max_blocks (the same row count).
+    bool dense = false;
 };
 
 // Arguments of one paged prefill attention launch (one layer). q / out hold the chunk tokens of
@@ -84,8 +88,10 @@ struct CopyArgs {
     size_t layer_bytes;     // num_blocks * block_bytes
 };
 
-// Partition geometry shared by the workspace query and the launch.
-int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks);
+// Partition geometry shared by the workspace query and the launch; sm_count is the device's
+// multiprocessor count (current_sm_count), so that the split fills the part it runs on.
+int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count);
+cudaError_t current_sm_count(int* out);
 inline int decode_partitions(int max_blocks, int bpp) { return (max_blocks + bpp - 1) / bpp; }
 
 // Split-K workspace layout (0 bytes when n_parts <= 1): fp32 partial outputs
@@ -123,6 +129,13 @@ cudaError_t launch_upload_metadata(void* dst, const void* src, size_t bytes, cud
 constexpr int kMmaMinGroup = 1;
 inline bool decode_uses_mma(int dtype, int group, long long rows) {
     return dtype != PKV_F32 && group >= kMmaMinGroup && rows < (1LL << 31);
+}
+
+// Status of a launcher's result: a pool address the tensor maps refused (not device memory of the
+// current device) is the caller's argument error; anything else from CUDA is PKV_ERR_CUDA.
+inline int launch_status(cudaError_t err) {
+    if (err == cudaSuccess) return PKV_OK;
+    return err == cudaErrorInvalidDevicePointer ? PKV_ERR_INVALID_ARG : PKV_ERR_CUDA;
 }
 
 // Cached TMA tensor map of one pool layer seen as rows x head_dim 16-bit elements (tmap.cu).

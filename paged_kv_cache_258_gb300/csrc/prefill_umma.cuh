@@ -63,17 +63,6 @@ __device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// The same copy delivered to the same shared-memory offset, and its bytes signalled to the mbarrier
-// at the same offset, in every CTA of `cta_mask` (one L2 read feeds several SMs).
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // 3-D tensor copy of one whole (block, KV head) chunk: box 64 columns x 16 rows x D/64 panels,
 // landing as [panel][16 rows][128 B] (tensor map of the PKV_BOX_BLOCK kind).
 __device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const void* tmap, int row, uint64_t* bar) {
@@ -81,15 +70,6 @@ __device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const void* tmap,
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const void* tmap, int row, uint64_t* bar,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar)), "h"(cta_mask)
         : "memory");
 }
 
@@ -155,11 +135,6 @@ struct UmmaTuning {
     // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (one issuing thread cannot
     // keep up with N = 64 instructions).
     static constexpr int BN = 128;
-    // CTAs per cluster sharing K/V loads: at head_dim 256 every CTA would pull 128 KiB per 128-key
-    // tile from L2 (the measured limit), so the four CTAs of a cluster, which hold adjacent query
-    // tiles of the same sequence and KV head, each load a quarter of every tile all of them need and
-    // multicast it to the four (measured: 825 TFLOP/s alone, 992 in pairs, 1,060 in fours).
-    static constexpr int CL = D == 256 ? 4 : 1;
     static constexpr bool PT = D <= 128;          // P in TMEM (A operand of PV) rather than shared memory
     static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
     static constexpr int STK = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K stages
@@ -241,7 +216,6 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::TADDR);
     const uint32_t sbase = smem_addr(smem);
 
-    constexpr int CL = Tu::CL;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // A launch that follows this one as a programmatic dependent (the next layer's attention of
@@ -266,37 +240,21 @@ __global__ void __launch_bounds__(256, 1)
         return (ctx - n_new + min(tq0 + QT, n_new) - 1) / BN + 1;
     };
     const int n_tiles = key_tiles(tile);
-    // tiles every CTA of the cluster needs (same sequence and KV head, adjacent query tiles)
-    const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
-    int n_common = 0;
-    if constexpr (CL > 1) {
-        n_common = n_tiles;
-        const int first = (int)(blockIdx.x & ~(unsigned)(CL - 1));  // the cluster's CTAs are consecutive in x
-#pragma unroll
-        for (int r = 0; r < CL; ++r) n_common = min(n_common, key_tiles(a.q_tiles - 1 - (first + r)));
-    }
-    if (n_tiles == 0) {
-        if constexpr (CL > 1) {  // still meet the other CTA at its two cluster barriers
-            cluster_sync_all();
-            cluster_sync_all();
-        }
-        return;
-    }
+    if (n_tiles == 0) return;
     const int t0 = tile * QT;
     const int pos0 = ctx - n_new + t0;
     const int nb = (ctx + kBlock - 1) / kBlock;
     const bool tail_tile = n_tiles * BN > ctx;  // the last tile holds rows past the context
 
     if (threadIdx.x == 0) {
-        // a stage is free again when the MMAs of every CTA that reads it are done with it: CL
-        // arrivals (the other CTA's by multicast commit; twice this CTA's for a tile only it reads)
+        // a stage is free again when the MMAs that read it are done with it (one commit)
         for (int i = 0; i < STK; ++i) {
             mbar_init(&full_k[i], 1);
-            mbar_init(&k_empty[i], CL);
+            mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < STV; ++i) {
             mbar_init(&full_v[i], 1);
-            mbar_init(&v_empty[i], CL);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
@@ -313,7 +271,6 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 5) tmem_alloc(taddr_s, Tu::TMEM_COLS);
     tcgen05_before_sync();
     __syncthreads();
-    if constexpr (CL > 1) cluster_sync_all();  // the other CTA's mbarriers exist before any multicast
     tcgen05_after_sync();
     const uint32_t tmem = *taddr_s;
 
@@ -370,26 +327,12 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (ok) {
                 const int row0 = (phys * a.n_kv + g) * kBlock;
-                // common tile: this CTA loads its share of the blocks into every CTA of the cluster
-                const bool mc = CL > 1 && j < n_common;
-                if (!mc || (uint32_t)lane * CL / (uint32_t)nbu == crank) {
-                    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
-                    if (is_v) {
-                        const uint32_t dst = sbase + ring + (uint32_t)st * VT + (uint32_t)lane * BLKB;
-                        if (mc)
-                            tma_load_3d_multicast(dst, tm, row0, &full[st], mask);
-                        else
-                            tma_load_3d_keep(dst, tm, row0, &full[st]);
-                    } else {
-                        const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
+                if (is_v) {
+                    tma_load_3d_keep(sbase + ring + (uint32_t)st * VT + (uint32_t)lane * BLKB, tm, row0, &full[st]);
+                } else {
+                    const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
 #pragma unroll
-                        for (int pn = 0; pn < PANELS; ++pn) {
-                            if (mc)
-                                tma_load_2d_multicast(dst + pn * PANEL, tm, pn * 64, row0, &full[st], mask);
-                            else
-                                tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
-                        }
-                    }
+                    for (int pn = 0; pn < PANELS; ++pn) tma_load_2d_keep(dst + pn * PANEL, tm, pn * 64, row0, &full[st]);
                 }
             }
             issued = u + 1;
@@ -422,16 +365,6 @@ __global__ void __launch_bounds__(256, 1)
         // 14-bit address field never carries).
         if (lane == 0) {
             bool ok = true;
-            // a stage of a common tile is released in every CTA of the cluster; a stage only this
-            // CTA reads gets all CL arrivals from here
-            auto release = [&](uint64_t* bar, int j) {
-                if (CL > 1 && j < n_common) {
-                    umma_commit_multicast(bar, (uint16_t)((1u << CL) - 1u));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < CL; ++c) umma_commit(bar);
-                }
-            };
             if (warp == 5) {
                 const uint64_t kdesc0 = umma_desc_sw128(sbase + (uint32_t)S::K, 16, 1024);
                 ok = mbar_wait_bounded(q_ready, 0u);
@@ -452,7 +385,7 @@ __global__ void __launch_bounds__(256, 1)
                                         kd + (uint64_t)(((uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32) >> 4),
                                         IDESC_S, ks > 0);
                     umma_commit(&s_full[b]);
-                    release(k_empty + st, j);  // the K stage may take tile j + STK once S_j is done
+                    umma_commit(&k_empty[st]);  // the K stage may take tile j + STK once S_j is done
                 }
             } else {
                 // V stage: block kk of the tile at + (kk % VB) * BLKB, its panels 2 KiB apart (leading
@@ -492,7 +425,7 @@ __global__ void __launch_bounds__(256, 1)
                             }
                         }
                         umma_commit(&p_free[pb * VPT + h]);  // part h of P buffer pb may take P_{j+NP}
-                        release(v_empty + sv, j);            // the V stage may take unit u + STV
+                        umma_commit(&v_empty[sv]);           // the V stage may take unit u + STV
                     }
                 }
             }
@@ -503,17 +436,6 @@ __global__ void __launch_bounds__(256, 1)
                 mbar_wait_bounded(&s_full[last % SB], (uint32_t)(last / SB) & 1u);
             else
                 mbar_wait_bounded(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u);
-            if constexpr (CL > 1) {
-                // and every release the other CTAs send here has landed: the last phase of each stage
-                // completes only with all of its arrivals
-                const int nst = warp == 5 ? STK : STV;
-                const int n_units = warp == 5 ? n_tiles : n_tiles * VPT;
-                uint64_t* empty = warp == 5 ? k_empty : v_empty;
-                for (int st = 0; st < nst && st < n_units; ++st) {
-                    const int ul = st + ((n_units - 1 - st) / nst) * nst;
-                    mbar_wait_bounded(&empty[st], (uint32_t)(ul / nst) & 1u);
-                }
-            }
         }
         __syncwarp();
     } else {
@@ -692,7 +614,6 @@ __global__ void __launch_bounds__(256, 1)
     }
     tcgen05_before_sync();
     __syncthreads();
-    if constexpr (CL > 1) cluster_sync_all();  // no CTA leaves while the other may still write to it
     if (warp == 5) {
         tcgen05_after_sync();
         tmem_dealloc(tmem, Tu::TMEM_COLS);
@@ -714,24 +635,17 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    constexpr int CL = UmmaTuning<D>::CL;
-    PrefillArgs b = a;
-    b.q_tiles = (a.q_tiles + CL - 1) / CL * CL;  // whole clusters; the extra query tiles have no rows
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(b.q_tiles, b.n_kv, b.n_seqs);
+    cfg.gridDim = dim3(a.q_tiles, a.n_kv, a.n_seqs);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.overlap_previous ? 2 : 1;
-    err = cudaLaunchKernelEx(&cfg, kern, b, tk, tv);
+    cfg.numAttrs = a.overlap_previous ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -12,7 +12,9 @@
 // runtime; maps are cached by (address, shape, type, box, device) in a hash table so steady-state
 // calls do not re-encode: a step touches up to 3 maps per layer (K panels, V panels, V blocks), so
 // the table holds every map of several multi-layer caches at once. A map depends only on its key,
-// so an entry stays valid even if its pool is freed and another one reuses the address.
+// so an entry stays valid even if its pool is freed and another one reuses the address. A new
+// address is accepted only if it is device memory of the current device
+// (cudaErrorInvalidDevicePointer otherwise, which the C ABI reports as PKV_ERR_INVALID_ARG).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -88,6 +90,14 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
         *out = hit->second;
         return cudaSuccess;
     }
+    // The copies read the pool directly: before a map is first built for an address, make sure it
+    // is device memory of this device (not host memory, not another GPU's memory).
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, layer_base) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is an argument error, not a sticky one
+        return cudaErrorInvalidDevicePointer;
+    }
+    if (pa.type != cudaMemoryTypeDevice || pa.device != dev) return cudaErrorInvalidDevicePointer;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     err = encoder(&encode);
     if (err != cudaSuccess) return err;

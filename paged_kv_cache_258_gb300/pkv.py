@@ -69,6 +69,8 @@ def lib():
         "pkv_bytes_per_token": (c_u64, [dp]),
         "pkv_pool_bytes": (c_u64, [dp]),
         "pkv_decode_workspace_bytes": (c_sz, [dp, c_i32, c_i32]),
+        "pkv_decode_split_geometry": (ctypes.c_int, [dp, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
+                                                     ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]),
         "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
         "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
                                                       vp, vp, c_sz, vp]),
@@ -78,6 +80,8 @@ def lib():
                                                                 ctypes.c_float, vp, vp, c_sz, c_u32, vp]),
         "pkv_paged_decode_attention_static": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32,
                                                              ctypes.c_float, vp, vp]),
+        "pkv_dense_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
+                                                      vp, vp, c_sz, c_u32, vp]),
         "pkv_paged_prefill_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
                                                        c_i32, ctypes.c_float, vp, vp]),
         "pkv_paged_prefill_attention_ex": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, vp, c_i32, c_i32,
@@ -86,6 +90,7 @@ def lib():
         "pkv_upload_metadata": (ctypes.c_int, [vp, vp, c_sz, vp]),
         "pkv_get_device_status": (ctypes.c_int, [vp, ctypes.POINTER(c_u32)]),
         "pkv_launch_count": (c_u64, []),
+        "pkv_hbm_read_probe": (ctypes.c_int, [vp, c_sz, vp, vp]),
         "pkv_selftest_wait_timeout": (ctypes.c_int, [vp]),
         "pkv_mgr_create": (vp, [c_i32, c_i32, vp]),
         "pkv_mgr_clone": (vp, [vp]),
@@ -149,9 +154,16 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on_current_device(x, name):
+    cur = _torch().cuda.current_device()
+    if x.device.index != cur:
+        raise ValueError(f"{name} is on {x.device}; the calls run on the current device, cuda:{cur}")
+
+
 def _dev(x, name, dtype=None, shape=None):
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(x, name)
     if not x.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and x.dtype != dtype:
@@ -179,6 +191,15 @@ def pkv_pool_bytes(desc: CacheDesc) -> int:
 
 def pkv_decode_workspace_bytes(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int) -> int:
     return int(lib().pkv_decode_workspace_bytes(ctypes.byref(desc), int(n_seqs), int(max_blocks_per_seq)))
+
+
+def pkv_decode_split_geometry(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, sm_count: int):
+    """(blocks per partition, partitions, workspace bytes) of decode on a part with sm_count SMs."""
+    bpp, nparts, nbytes = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_size_t(0)
+    _check(lib().pkv_decode_split_geometry(ctypes.byref(desc), int(n_seqs), int(max_blocks_per_seq), int(sm_count),
+                                           ctypes.byref(bpp), ctypes.byref(nparts), ctypes.byref(nbytes)),
+           "pkv_decode_split_geometry")
+    return int(bpp.value), int(nparts.value), int(nbytes.value)
 
 
 def pkv_kv_append(desc: CacheDesc, layer: int, k, v, slot_mapping, k_pool, v_pool, stream=None) -> None:
@@ -214,6 +235,34 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
         _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
         _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
     _check(rc, "pkv_paged_decode_attention")
+
+
+def dense_cache_shape(desc: CacheDesc, n_seqs: int, max_seq_len: int):
+    """[n_layers, n_seqs, n_kv, max_seq_len, d]: the dense (batch, heads, length, head_dim) cache."""
+    return (desc.n_layers, n_seqs, desc.n_kv_heads, max_seq_len, desc.head_dim)
+
+
+def pkv_dense_decode_attention(desc: CacheDesc, layer: int, q, k_cache, v_cache, context_lens, scale: float, out,
+                               workspace=None, stream=None, overlap_previous: bool = False) -> None:
+    """Decode attention over a dense cache [L, n_seqs, n_kv, S, d] (identity walk, no block table)."""
+    t = _torch()
+    dt = torch_dtype(desc.dtype_name)
+    n_seqs = int(q.shape[0])
+    if k_cache.dim() != 5:
+        raise ValueError("k_cache must be [n_layers, n_seqs, n_kv, max_seq_len, head_dim]")
+    s_max = int(k_cache.shape[3])
+    shape = dense_cache_shape(desc, n_seqs, s_max)
+    qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pkv_dense_decode_attention(
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape), _dev(k_cache, "k_cache", dt, shape),
+        _dev(v_cache, "v_cache", dt, shape), s_max, _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs,
+        float(scale), _dev(out, "out", dt, qshape), ws_ptr, ws_bytes,
+        PKV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0, _stream_handle(stream))
+    _check(rc, "pkv_dense_decode_attention")
 
 
 def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_new, k_pool, v_pool, block_tables,
@@ -343,6 +392,7 @@ def _layered(x, name, dtype, n_layers: int, row_shape):
     """(address of layer 0, bytes between layers) of a [n_layers, *row_shape] tensor."""
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(x, name)
     if x.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
     if tuple(x.shape) != (n_layers, *row_shape):
@@ -437,6 +487,17 @@ def pkv_get_device_status(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pkv_get_device_status(_stream_handle(stream), ctypes.byref(flags)), "pkv_get_device_status")
     return int(flags.value)
+
+
+def pkv_hbm_read_probe(buf, fold, stream=None) -> None:
+    """Stream every byte of the device tensor buf once; XOR-fold its 32-bit words into fold (a
+    device int32 tensor of one element)."""
+    if not buf.is_contiguous():
+        raise ValueError("buf must be contiguous")
+    _on_current_device(buf, "buf")
+    _check(lib().pkv_hbm_read_probe(ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size(),
+                                    _dev(fold, "fold", _torch().int32, (1,)), _stream_handle(stream)),
+           "pkv_hbm_read_probe")
 
 
 def pkv_launch_count() -> int:

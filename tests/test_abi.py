@@ -58,14 +58,39 @@ def test_validate_desc(kw, want):
     assert pkv.pkv_validate_desc(pkv.make_desc(**kw)) == want
 
 
+def _ws(desc, n_seqs, max_blocks, sms=152):
+    return pkv.pkv_decode_split_geometry(desc, n_seqs, max_blocks, sms)[2]
+
+
 def test_workspace_only_when_split():
     d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)
-    assert pkv.pkv_decode_workspace_bytes(d, 64, 64) == 0          # one partition per sequence
-    n = pkv.pkv_decode_workspace_bytes(d, 64, 129)
+    assert _ws(d, 64, 64) == 0                                      # one partition per sequence
+    n = _ws(d, 64, 129)
     assert n == 64 * 32 * 3 * (128 + 2) * 4 + 64 * 32 * 8          # 129 blocks -> 3 partitions of 64
     d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)
-    assert pkv.pkv_decode_workspace_bytes(d4, 10, 2048) == 10 * 16 * 32 * (256 + 2) * 4 + 10 * 4 * 8
+    assert _ws(d4, 10, 2048) == 10 * 16 * 32 * (256 + 2) * 4 + 10 * 4 * 8
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_decode_split_geometry(d, 0, 10, 152)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_decode_split_geometry(d, 4, 10, 0)
     assert pkv.pkv_decode_workspace_bytes(d, 0, 10) == 0
+
+
+def test_split_geometry_follows_the_sm_count():
+    """Partitions shrink until the grid holds at least 4 CTAs per SM of the part it runs on."""
+    d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)      # 10 sequences x 4 KV heads x 2,048 blocks
+    for sms, bpp in [(152, 64), (76, 64), (20, 64), (304, 64), (400, 32), (1000, 16), (4000, 4), (10 ** 6, 4)]:
+        got_bpp, n_parts, nbytes = pkv.pkv_decode_split_geometry(d4, 10, 2048, sms)
+        assert got_bpp == bpp, sms
+        assert n_parts == -(-2048 // bpp)
+        assert 10 * 4 * n_parts >= 4 * sms or bpp == 4      # the target, unless partitions are minimal
+        assert nbytes == 10 * 16 * n_parts * (256 + 2) * 4 + 10 * 4 * 8
+    d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)          # gpt-like: 64 x 32 CTAs already fill 152 SMs
+    assert pkv.pkv_decode_split_geometry(d, 64, 129, 152)[:2] == (64, 3)
+    assert pkv.pkv_decode_split_geometry(d, 64, 129, 2048)[:2] == (32, 5)
+    # a single sequence and head is spread as far as 4-block partitions allow, whatever the part
+    one = pkv.make_desc("f16", 1, 4096, 1, 1, 128)
+    assert pkv.pkv_decode_split_geometry(one, 1, 128, 8)[:2] == (4, 32)
 
 
 def test_device_calls_reject_bad_arguments_before_launch():

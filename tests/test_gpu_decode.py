@@ -259,3 +259,68 @@ def test_bounded_wait_gives_up_and_context_stays_usable():
     assert 0.5 < waited < 10.0
     assert pkv.pkv_get_device_status() == 0          # reading cleared it
     check("f16", [5, 40, 300], 4, 2, 64, seed=31)     # the context is still healthy
+
+
+def test_workspace_query_and_launch_use_the_devices_sm_count():
+    """The workspace query reads this device's SM count; a workspace of exactly that size is
+    accepted and one byte less is refused before launch, so query and launch agree."""
+    import ctypes
+
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    lens = [3000, 17, 900]
+    q, kp, vp, tables, lens, nb = paged_case("bf16", lens, 16, 4, 256, seed=77)
+    desc = pkv.make_desc("bf16", 1, nb, 16, 4, 256)
+    mb = tables.shape[1]
+    need = pkv.pkv_decode_workspace_bytes(desc, len(lens), mb)
+    assert need == pkv.pkv_decode_split_geometry(desc, len(lens), mb, sms)[2] > 0
+    k_t, v_t, q_t = to_torch(kp, "bf16"), to_torch(vp, "bf16"), to_torch(q, "bf16")
+    t_t = torch.from_numpy(np.ascontiguousarray(tables)).cuda()
+    l_t = torch.from_numpy(lens).cuda()
+    ws = torch.zeros(need // 4 + 4, dtype=torch.float32, device="cuda")
+    out = torch.full_like(q_t, float("nan"))
+    L = pkv.lib()
+    vp_ = ctypes.c_void_p
+
+    def call(nbytes):
+        return L.pkv_paged_decode_attention(ctypes.byref(desc), 0, vp_(q_t.data_ptr()), vp_(k_t.data_ptr()),
+                                            vp_(v_t.data_ptr()), vp_(t_t.data_ptr()), mb, vp_(l_t.data_ptr()),
+                                            len(lens), ctypes.c_float(1 / 16), vp_(out.data_ptr()),
+                                            vp_(ws.data_ptr()), nbytes, vp_(0))
+    assert call(need - 1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(need) == pkv.PKV_OK
+    assert pkv.pkv_get_device_status() == 0
+    want = oracle.paged_decode("bf16", q, kp[0], vp[0], tables, lens, 1 / 16)
+    assert np.max(np.abs(as_f64(out) - want)) <= TOL["bf16"]
+
+
+def test_pools_on_the_host_are_refused_before_launch():
+    """The tensor copies read the pools directly: host memory is refused (PKV_ERR_INVALID_ARG)."""
+    import ctypes
+
+    import torch
+    q, kp, vp, tables, lens, nb = paged_case("f16", [40, 70], 4, 4, 64, seed=78)
+    desc = pkv.make_desc("f16", 1, nb, 4, 4, 64)
+    k_host = torch.from_numpy(np.ascontiguousarray(kp)).pin_memory()
+    v_t, q_t = to_torch(vp, "f16"), to_torch(q, "f16")
+    t_t = torch.from_numpy(np.ascontiguousarray(tables)).cuda()
+    l_t = torch.from_numpy(lens).cuda()
+    qs = torch.tensor([0, 40, 80], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q_t)
+    before = pkv.pkv_launch_count()
+    L = pkv.lib()
+    vp_ = ctypes.c_void_p
+    rc = L.pkv_paged_decode_attention(ctypes.byref(desc), 0, vp_(q_t.data_ptr()), vp_(k_host.data_ptr()),
+                                      vp_(v_t.data_ptr()), vp_(t_t.data_ptr()), tables.shape[1],
+                                      vp_(l_t.data_ptr()), 2, ctypes.c_float(0.125), vp_(out.data_ptr()),
+                                      vp_(0), 0, vp_(0))
+    assert rc == pkv.PKV_ERR_INVALID_ARG
+    q80 = torch.zeros((80, 4, 64), dtype=torch.float16, device="cuda")
+    o80 = torch.empty_like(q80)
+    rc = L.pkv_paged_prefill_attention(ctypes.byref(desc), 0, vp_(q80.data_ptr()), vp_(k_host.data_ptr()),
+                                       vp_(v_t.data_ptr()), vp_(t_t.data_ptr()), tables.shape[1],
+                                       vp_(l_t.data_ptr()), vp_(qs.data_ptr()), 2, 80, 40, ctypes.c_float(0.125),
+                                       vp_(o80.data_ptr()), vp_(0))
+    assert rc == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.pkv_launch_count() == before
+    assert pkv.pkv_get_device_status() == 0

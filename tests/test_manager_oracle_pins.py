@@ -147,3 +147,145 @@ def test_error_statuses():
     assert m.free_seq(5) == "ok"
     assert m.free_seq(5) == "invalid"             # double free
     assert m.stats()["free_blocks"] == 2
+
+
+# ---- extend by a chunk (chunked prefill, "01 - Conceito" paragraph 5) --------------------------
+# The reading: a chunk of n tokens is all or nothing, and when it is admitted it equals n single
+# appends of "La idea de PagedAttention" step 3. The pin below checks exactly that against the
+# single-append path (itself pinned above), never against extend's own block arithmetic: extend(s, n)
+# is "ok" iff n successive append_slot(s) calls on a deep copy all succeed, and then the two
+# managers are equal (tables, lengths, reference counts, free-list order, counters), the slots
+# agree and the one copy-on-write pair, if any, is the appends' pair.
+
+import copy  # noqa: E402
+
+
+def full_state(m: BlockManagerOracle):
+    return snapshot(m) + (m.alloc_failures, m.prefix_hits, m.cow_copies, m.append_oom)
+
+
+def extend_agrees_with_appends(m: BlockManagerOracle, seq: int, n: int) -> bool:
+    """True when extend(seq, n) on a copy of m behaves like n appends on another copy."""
+    ref = copy.deepcopy(m)
+    slots, pairs, ok = [], [], True
+    for _ in range(n):
+        st, slot, src, dst = ref.append_slot(seq)
+        if st != "ok":
+            ok = False
+            break
+        slots.append(slot)
+        if src >= 0:
+            pairs.append((src, dst))
+    ext = copy.deepcopy(m)
+    before = full_state(ext)
+    try:
+        st, got_slots, src, dst = ext.extend(seq, n)
+    except AssertionError:      # a wrong admission test lets the chunk run out of blocks midway
+        return False
+    if not ok:
+        # refused: nothing moves but one allocation failure and one append OOM
+        want = before[:-4] + (before[-4] + 1, before[-3], before[-2], before[-1] + 1)
+        return st == "no_blocks" and full_state(ext) == want
+    if st != "ok" or got_slots != slots or full_state(ext) != full_state(ref) or len(pairs) > 1:
+        return False
+    return (src, dst) == (pairs[0] if pairs else (-1, -1))
+
+
+def random_manager(rng: random.Random):
+    """A seeded manager state with shared prefixes, shared partial tails and a small free list."""
+    nb = rng.randint(6, 40)
+    m = BlockManagerOracle(nb, free_order=rng.sample(range(nb), nb))
+    next_id = 0
+    for _ in range(rng.randint(2, 30)):
+        live = list(m.tables)
+        r = rng.random()
+        if r < 0.35 or not live:
+            m.add_seq(next_id, rng.randint(0, 60))
+            next_id += 1
+        elif r < 0.6:
+            m.fork(rng.choice(live), next_id)    # shares every block, the partial tail included
+            next_id += 1
+        elif r < 0.9:
+            m.append_slot(rng.choice(live))
+        else:
+            m.free_seq(rng.choice(live))
+    return m
+
+
+def boundary_chunks(m: BlockManagerOracle, seq: int):
+    """Chunk sizes around the largest chunk the pool can hold (found by single appends)."""
+    ref = copy.deepcopy(m)
+    fit = 0
+    while ref.append_slot(seq)[0] == "ok":
+        fit += 1
+    return sorted({0, 1, 2, BS - 1, BS, BS + 1, max(fit - BS, 0), max(fit - 1, 0), fit, fit + 1, fit + 2,
+                   fit + BS})
+
+
+def test_extend_equals_successive_appends_at_the_admission_boundary():
+    rng = random.Random(2024)
+    n_checked = n_refused = n_cow = 0
+    for _ in range(400):
+        m = random_manager(rng)
+        if not m.tables:
+            continue
+        for seq in list(m.tables):
+            shared_tail = m.ctx[seq] % BS != 0 and m.ref[m.tables[seq][-1]] > 1
+            for n in boundary_chunks(m, seq):
+                assert extend_agrees_with_appends(m, seq, n), (seq, n)
+                n_checked += 1
+                probe = copy.deepcopy(m)
+                st = probe.extend(seq, n)[0]
+                n_refused += st == "no_blocks"
+                n_cow += st == "ok" and n > 0 and shared_tail
+    assert n_checked > 2000 and n_refused > 300 and n_cow > 100   # both sides of the boundary, with CoW
+
+
+def _planted_extend(m, seq_id, n_tokens, slack: int, cow_block: bool):
+    """extend with its admission test altered: `slack` extra blocks believed free, and the copy-on-
+    write block counted only if cow_block. The rest follows the oracle's steps."""
+    if seq_id not in m.tables or n_tokens <= 0:
+        return BlockManagerOracle.extend(m, seq_id, n_tokens)
+    cow = m.ctx[seq_id] % BS != 0 and m.ref[m.tables[seq_id][-1]] > 1
+    need = -(-(m.ctx[seq_id] + n_tokens) // BS) - len(m.tables[seq_id]) + (1 if cow and cow_block else 0)
+    if need > len(m.free) + slack:
+        m.alloc_failures += 1
+        m.append_oom += 1
+        return "no_blocks", [], -1, -1
+    slots, src, dst = [], -1, -1
+    for _ in range(n_tokens):
+        st, slot, s_, d_ = m.append_slot(seq_id)
+        assert st == "ok"
+        slots.append(slot)
+        if s_ >= 0:
+            src, dst = s_, d_
+    return "ok", slots, src, dst
+
+
+class _OffByOne(BlockManagerOracle):
+    """Planted mistake: admits a chunk that needs one block more than the pool holds."""
+
+    def extend(self, seq_id, n_tokens):
+        return _planted_extend(self, seq_id, n_tokens, slack=1, cow_block=True)
+
+
+class _NoCowBlock(BlockManagerOracle):
+    """Planted mistake: forgets the extra block a copy-on-write first token takes."""
+
+    def extend(self, seq_id, n_tokens):
+        return _planted_extend(self, seq_id, n_tokens, slack=0, cow_block=False)
+
+
+@pytest.mark.parametrize("mutant", [_OffByOne, _NoCowBlock])
+def test_extend_pin_catches_planted_mistakes(mutant):
+    """The pin above has teeth: each planted admission mistake breaks it on some seeded state."""
+    rng = random.Random(2024)
+    for _ in range(400):
+        m = random_manager(rng)
+        bad = mutant(m.num_blocks)
+        bad.__dict__.update(copy.deepcopy(m.__dict__))
+        for seq in list(bad.tables):
+            for n in boundary_chunks(bad, seq):
+                if not extend_agrees_with_appends(bad, seq, n):
+                    return
+    pytest.fail(f"{mutant.__name__} was not caught")
