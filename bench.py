@@ -422,8 +422,85 @@ def measure_decode(args, config: str, device, rank: int, ws: int, read_peak: dic
     return res
 
 
+def measure_dense(args, config: str, device, rank: int, read_peak: dict | None) -> dict:
+    """The same decode kernels over a dense (batch, heads, max length, head_dim) cache with the same
+    context lengths ("Lo que funciona en la Fase 22" keeps such a cache; the identity walk replaces
+    the table). A step = one pkv_dense_decode_attention per layer, chained as in the paged step;
+    value = KV bytes read / step time; roofline = each launch alone between CUDA events."""
+    import torch
+    from paged_kv_cache_258_gb300 import pkv
+
+    wl, wdesc, churn = build_workload(config, args.warmup, args.steps, rank, args.layers)
+    if churn is not None:
+        raise ValueError("the dense comparison needs a fixed batch (gpt, ragged, longdoc)")
+    L, B, n_kv, d = wl.n_layers, wl.n_seqs, wl.n_kv_heads, wl.head_dim
+    lens = wl.context_lens.astype(np.int32)
+    s_max = int(-(-int(lens.max()) // W.BLOCK) * W.BLOCK)
+    desc = pkv.make_desc(wl.dtype, L, 1, wl.n_q_heads, n_kv, d)
+    dt = pkv.torch_dtype(wl.dtype)
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed + 23)
+    shape = pkv.dense_cache_shape(desc, B, s_max)
+    k_cache = torch.randn(shape, dtype=dt, device=device, generator=g)
+    v_cache = torch.randn(shape, dtype=dt, device=device, generator=g)
+    q = torch.randn((L, B, wl.n_q_heads, d), dtype=dt, device=device, generator=g)
+    out = torch.empty_like(q)
+    l_t = torch.from_numpy(lens).to(device)
+    ws_t = pkv.alloc_workspace(desc, B, s_max // W.BLOCK, device=device)
+    stream = torch.cuda.current_stream(device)
+    step_bytes = int(lens.astype(np.int64).sum()) * 2 * n_kv * d * wl.elem_bytes * L
+
+    def step(events=None):
+        for layer in range(L):
+            if events is not None:
+                events[layer][0].record(stream)
+            pkv.pkv_dense_decode_attention(desc, layer, q[layer], k_cache, v_cache, l_t, wl.scale, out[layer], ws_t,
+                                           stream, overlap_previous=events is None and layer > 0)
+            if events is not None:
+                events[layer][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    if pkv.pkv_get_device_status(stream):
+        raise RuntimeError(f"device status flags set during the dense pass ({config})")
+    ms = t0.elapsed_time(t1)
+    durs = [a.elapsed_time(b) for row in evs for a, b in row]
+    per_launch = step_bytes / L / (sum(durs) / len(durs) * 1e-3) / 1e9
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    res = {"value": round(step_bytes * args.steps / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "ms_per_step": round(ms / args.steps, 4),
+           "layout": f"dense [{L}][{B}][{n_kv}][{s_max}][{d}] per K and V, identity walk",
+           "roofline": {"achieved": round(per_launch, 2), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(per_launch / hbm_peak, 4), "launch_ms_mean": round(sum(durs) / len(durs), 5)}}
+    if read_peak:
+        res["roofline"]["frac_of_read_peak"] = round(per_launch / read_peak["best_gbs"], 4)
+    del k_cache, v_cache, q, out, ws_t
+    return res
+
+
+def indirection(paged: dict, dense: dict) -> dict:
+    """The constant factor of the table walk: 1 - paged / dense, per step and per launch."""
+    return {"step": round(1.0 - paged["value"] / dense["value"], 4),
+            "per_launch": round(1.0 - paged["roofline"]["achieved"] / dense["roofline"]["achieved"], 4),
+            "note": "fraction of the dense cache's bandwidth lost to the block-table walk and scattered placement"}
+
+
 # the target workloads measured beside the headline one in the default run (one line, keyed objects)
 SUB_CONFIGS = ("longdoc", "ragged", "prefix")
+DENSE_CONFIGS = ("gpt", "longdoc")  # the dense-cache comparison of the default run
 
 
 def run_gpu(args) -> dict | None:
@@ -439,13 +516,24 @@ def run_gpu(args) -> dict | None:
     pkv.lib()
     read_peak = measure_read_peak(device)
     cpu = ws == 1 and not args.no_cpu_baseline
-    res = measure_decode(args, args.config, device, rank, ws, read_peak, cpu, args.cpu_budget)
+    dense_for = set(DENSE_CONFIGS) if args.dense == "auto" else ({args.config} if args.dense == "on" else set())
+
+    def one(name, budget):
+        r = measure_decode(args, name, device, rank, ws, read_peak, cpu, budget)
+        if name in dense_for and args.placement == "shuffled":
+            gc.collect()
+            torch.cuda.empty_cache()
+            r["dense"] = measure_dense(args, name, device, rank, read_peak)
+            r["indirection_overhead"] = indirection(r, r["dense"])
+        return r
+
+    res = one(args.config, args.cpu_budget)
     subs = {}
     if args.config == "gpt" and not args.no_sub_configs and args.layers is None:
         for name in SUB_CONFIGS:
             gc.collect()
             torch.cuda.empty_cache()
-            subs[name] = measure_decode(args, name, device, rank, ws, read_peak, cpu, min(args.cpu_budget, 6.0))
+            subs[name] = one(name, min(args.cpu_budget, 6.0))
     if rank != 0:
         return None
     line = {
@@ -1351,6 +1439,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-configs", action="store_true",
                     help="gpt only: skip the longdoc / ragged / prefix measurements of the default run")
+    ap.add_argument("--dense", default="auto", choices=["auto", "on", "off"],
+                    help="time the same kernels over a dense (B, H, S, d) cache beside the paged pool: "
+                         "auto = gpt and longdoc, on = this config too, off = never")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling)")
     ap.add_argument("--placement", default="shuffled", choices=["shuffled", "contiguous"],
                     help="physical placement of each sequence's blocks (indirection-overhead study)")

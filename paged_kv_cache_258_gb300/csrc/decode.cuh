@@ -72,6 +72,7 @@ __device__ __forceinline__ long long chunk_index(const DecodeArgs& a, int s, int
 }
 
 constexpr int kMergeChunk = 32;  // partitions whose weights are staged in shared memory at a time
+constexpr int kMergeLoads = 64;  // partial-output loads a merging thread keeps in flight at once
 
 // Shared-memory floats the split-K merge needs (flag, row maxima, row sums, one chunk of weights).
 template <int G>
@@ -109,6 +110,7 @@ __device__ __forceinline__ void splitk_merge_if_last(const DecodeArgs& a, int s,
     static_assert(NT % 32 == 0, "whole warps");
     constexpr int NWARP = NT / 32;
     constexpr int PER = (G * D + NT - 1) / NT;
+    constexpr int MQ = kMergeLoads / PER < 2 ? 2 : (kMergeLoads / PER > 16 ? 16 : kMergeLoads / PER);
     int* flag = reinterpret_cast<int*>(scratch);
     float* sM = scratch + 4;  // [G]
     float* sL = sM + G;       // [G]
@@ -167,14 +169,31 @@ __device__ __forceinline__ void splitk_merge_if_last(const DecodeArgs& a, int s,
         }
         __syncthreads();
         const int nq = min(kMergeChunk, np - c0);
+        // The partials are read in groups of MQ: every thread first issues the MQ x PER loads of a
+        // group (all independent, all in flight at once), then folds them in partition order. The
+        // merging CTA ends the (sequence, KV head) -- often the whole launch -- so its reads must
+        // not wait on each other one L2 round trip at a time. Same FMA order as a plain loop.
+        for (int q0 = 0; q0 < nq; q0 += MQ) {
+            const int mq = min(MQ, nq - q0);
+            float v[PER][MQ];
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int idx = threadIdx.x + k * NT;
-            if (idx < G * D) {
+            for (int k = 0; k < PER; ++k) {
+                const int idx = threadIdx.x + k * NT;
                 const int r = idx / D;
-                const int d = idx % D;
-                const float* po = a.part_o + ((row0 + r) * a.n_parts + c0) * D + d;
-                for (int q = 0; q < nq; ++q) O[k] = fmaf(sW[r * kMergeChunk + q], __ldcg(po + (size_t)q * D), O[k]);
+                const float* po = a.part_o + ((row0 + r) * a.n_parts + c0 + q0) * D + idx % D;
+#pragma unroll
+                for (int u = 0; u < MQ; ++u)
+                    v[k][u] = (idx < G * D && u < mq) ? __ldcg(po + (size_t)u * D) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int idx = threadIdx.x + k * NT;
+                if (idx < G * D) {
+                    const float* w = sW + (idx / D) * kMergeChunk + q0;
+#pragma unroll
+                    for (int u = 0; u < MQ; ++u)
+                        if (u < mq) O[k] = fmaf(w[u], v[k][u], O[k]);
+                }
             }
         }
     }

@@ -154,16 +154,28 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _on_current_device(x, name):
-    cur = _torch().cuda.current_device()
-    if x.device.index != cur:
+def _current_device() -> int:
+    """Index of the current CUDA device, or -1 where CUDA cannot be initialised (every tensor check
+    then fails on its own, with a ValueError, before any launch)."""
+    try:
+        return _torch().cuda.current_device()
+    except (RuntimeError, AssertionError):
+        return -1
+
+
+def _on_current_device(x, name, cur=None):
+    """The library runs on the current device: a tensor elsewhere is refused. `cur` (the current
+    device's index) is read once per call by callers that check several tensors."""
+    if cur is None:
+        cur = _torch().cuda.current_device()
+    if x.get_device() != cur:
         raise ValueError(f"{name} is on {x.device}; the calls run on the current device, cuda:{cur}")
 
 
-def _dev(x, name, dtype=None, shape=None):
+def _dev(x, name, dtype=None, shape=None, cur=None):
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    _on_current_device(x, name)
+    _on_current_device(x, name, cur)
     if not x.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and x.dtype != dtype:
@@ -205,12 +217,13 @@ def pkv_decode_split_geometry(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: 
 def pkv_kv_append(desc: CacheDesc, layer: int, k, v, slot_mapping, k_pool, v_pool, stream=None) -> None:
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_tok = int(k.shape[0])
     row = (n_tok, desc.n_kv_heads, desc.head_dim)
     rc = lib().pkv_kv_append(
-        ctypes.byref(desc), int(layer), _dev(k, "k", dt, row), _dev(v, "v", dt, row),
-        _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,)), n_tok,
-        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
+        ctypes.byref(desc), int(layer), _dev(k, "k", dt, row, cur=cur), _dev(v, "v", dt, row, cur=cur),
+        _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,), cur=cur), n_tok,
+        _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur), _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
         _stream_handle(stream))
     _check(rc, "pkv_kv_append")
 
@@ -219,6 +232,7 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
                                scale: float, out, workspace=None, stream=None) -> None:
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_seqs = int(q.shape[0])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
@@ -226,14 +240,14 @@ def pkv_paged_decode_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, b
     qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
-        ws_ptr = _dev(workspace, "workspace")
+        ws_ptr = _dev(workspace, "workspace", cur=cur)
         ws_bytes = workspace.numel() * workspace.element_size()
     rc = lib().pkv_paged_decode_attention(
-        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
-        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
-        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
-        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
-        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes, _stream_handle(stream))
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape, cur=cur),
+        _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur), _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks), cur=cur), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape, cur=cur), ws_ptr, ws_bytes, _stream_handle(stream))
     _check(rc, "pkv_paged_decode_attention")
 
 
@@ -247,6 +261,7 @@ def pkv_dense_decode_attention(desc: CacheDesc, layer: int, q, k_cache, v_cache,
     """Decode attention over a dense cache [L, n_seqs, n_kv, S, d] (identity walk, no block table)."""
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_seqs = int(q.shape[0])
     if k_cache.dim() != 5:
         raise ValueError("k_cache must be [n_layers, n_seqs, n_kv, max_seq_len, head_dim]")
@@ -255,12 +270,12 @@ def pkv_dense_decode_attention(desc: CacheDesc, layer: int, q, k_cache, v_cache,
     qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
-        ws_ptr = _dev(workspace, "workspace")
+        ws_ptr = _dev(workspace, "workspace", cur=cur)
         ws_bytes = workspace.numel() * workspace.element_size()
     rc = lib().pkv_dense_decode_attention(
-        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape), _dev(k_cache, "k_cache", dt, shape),
-        _dev(v_cache, "v_cache", dt, shape), s_max, _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs,
-        float(scale), _dev(out, "out", dt, qshape), ws_ptr, ws_bytes,
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape, cur=cur), _dev(k_cache, "k_cache", dt, shape, cur=cur),
+        _dev(v_cache, "v_cache", dt, shape, cur=cur), s_max, _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur), n_seqs,
+        float(scale), _dev(out, "out", dt, qshape, cur=cur), ws_ptr, ws_bytes,
         PKV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0, _stream_handle(stream))
     _check(rc, "pkv_dense_decode_attention")
 
@@ -275,6 +290,7 @@ def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_n
     """
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_seqs = int(q.shape[0])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
@@ -283,15 +299,15 @@ def pkv_paged_decode_append_attention(desc: CacheDesc, layer: int, q, k_new, v_n
     kvshape = (n_seqs, desc.n_kv_heads, desc.head_dim)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None:
-        ws_ptr = _dev(workspace, "workspace")
+        ws_ptr = _dev(workspace, "workspace", cur=cur)
         ws_bytes = workspace.numel() * workspace.element_size()
     rc = lib().pkv_paged_decode_append_attention_ex(
-        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape), _dev(k_new, "k_new", dt, kvshape),
-        _dev(v_new, "v_new", dt, kvshape), _dev(k_pool, "k_pool", dt, pool_shape(desc)),
-        _dev(v_pool, "v_pool", dt, pool_shape(desc)),
-        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
-        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
-        _dev(out, "out", dt, qshape), ws_ptr, ws_bytes,
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape, cur=cur), _dev(k_new, "k_new", dt, kvshape, cur=cur),
+        _dev(v_new, "v_new", dt, kvshape, cur=cur), _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur),
+        _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks), cur=cur), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape, cur=cur), ws_ptr, ws_bytes,
         PKV_DECODE_OVERLAP_PREVIOUS if overlap_previous else 0, _stream_handle(stream))
     _check(rc, "pkv_paged_decode_append_attention")
 
@@ -305,17 +321,18 @@ def pkv_paged_decode_attention_static(desc: CacheDesc, layer: int, q, k_pool, v_
     """
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_seqs = int(q.shape[0])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
     max_blocks = int(block_tables.shape[1])
     qshape = (n_seqs, desc.n_q_heads, desc.head_dim)
     rc = lib().pkv_paged_decode_attention_static(
-        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
-        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
-        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
-        _dev(context_lens, "context_lens", t.int32, (n_seqs,)), n_seqs, float(scale),
-        _dev(out, "out", dt, qshape), _stream_handle(stream))
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape, cur=cur),
+        _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur), _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks), cur=cur), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur), n_seqs, float(scale),
+        _dev(out, "out", dt, qshape, cur=cur), _stream_handle(stream))
     _check(rc, "pkv_paged_decode_attention_static")
 
 
@@ -331,18 +348,19 @@ def pkv_paged_prefill_attention(desc: CacheDesc, layer: int, q, k_pool, v_pool, 
     """
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_tokens = int(q.shape[0])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
     n_seqs, max_blocks = int(block_tables.shape[0]), int(block_tables.shape[1])
     qshape = (n_tokens, desc.n_q_heads, desc.head_dim)
     rc = lib().pkv_paged_prefill_attention_ex(
-        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape),
-        _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
-        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks)), max_blocks,
-        _dev(context_lens, "context_lens", t.int32, (n_seqs,)),
-        _dev(query_start, "query_start", t.int32, (n_seqs + 1,)), n_seqs, n_tokens, int(max_query_len),
-        float(scale), _dev(out, "out", dt, qshape), PKV_PREFILL_OVERLAP_PREVIOUS if overlap_previous else 0,
+        ctypes.byref(desc), int(layer), _dev(q, "q", dt, qshape, cur=cur),
+        _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur), _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
+        _dev(block_tables, "block_tables", t.int32, (n_seqs, max_blocks), cur=cur), max_blocks,
+        _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur),
+        _dev(query_start, "query_start", t.int32, (n_seqs + 1,), cur=cur), n_seqs, n_tokens, int(max_query_len),
+        float(scale), _dev(out, "out", dt, qshape, cur=cur), PKV_PREFILL_OVERLAP_PREVIOUS if overlap_previous else 0,
         _stream_handle(stream))
     _check(rc, "pkv_paged_prefill_attention")
 
@@ -355,10 +373,11 @@ def pkv_selftest_wait_timeout(stream=None) -> None:
 def pkv_copy_blocks(desc: CacheDesc, k_pool, v_pool, pairs, stream=None) -> None:
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     n_pairs = int(pairs.shape[0])
     rc = lib().pkv_copy_blocks(
-        ctypes.byref(desc), _dev(k_pool, "k_pool", dt, pool_shape(desc)), _dev(v_pool, "v_pool", dt, pool_shape(desc)),
-        _dev(pairs, "pairs", t.int32, (n_pairs, 2)), n_pairs, _stream_handle(stream))
+        ctypes.byref(desc), _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur), _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur),
+        _dev(pairs, "pairs", t.int32, (n_pairs, 2), cur=cur), n_pairs, _stream_handle(stream))
     _check(rc, "pkv_copy_blocks")
 
 
@@ -388,11 +407,11 @@ def upload_metadata_ptr(dst_ptr: int, src_ptr: int, nbytes: int, stream_handle: 
 # fine) and keep raw addresses, so a layer's launch is a single call into the C ABI with the same
 # arguments the per-call bindings above would pass.
 
-def _layered(x, name, dtype, n_layers: int, row_shape):
+def _layered(x, name, dtype, n_layers: int, row_shape, cur=None):
     """(address of layer 0, bytes between layers) of a [n_layers, *row_shape] tensor."""
     if not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    _on_current_device(x, name)
+    _on_current_device(x, name, cur)
     if x.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
     if tuple(x.shape) != (n_layers, *row_shape):
@@ -412,19 +431,20 @@ def decode_append_launcher(desc: CacheDesc, q, k_new, v_new, k_pool, v_pool, blo
     q/out [L, n, n_q, d] and k_new/v_new [L, n, n_kv, d] validated here once."""
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     L, n = desc.n_layers, int(q.shape[1])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
     mb = int(block_tables.shape[1])
-    q0, qs = _layered(q, "q", dt, L, (n, desc.n_q_heads, desc.head_dim))
-    o0, os_ = _layered(out, "out", dt, L, (n, desc.n_q_heads, desc.head_dim))
-    k0, ks = _layered(k_new, "k_new", dt, L, (n, desc.n_kv_heads, desc.head_dim))
-    v0, vs = _layered(v_new, "v_new", dt, L, (n, desc.n_kv_heads, desc.head_dim))
-    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
-    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
-    tb = _dev(block_tables, "block_tables", t.int32, (n, mb)).value
-    ln = _dev(context_lens, "context_lens", t.int32, (n,)).value
-    wsp, wsb = (None, 0) if workspace is None else (_dev(workspace, "workspace").value,
+    q0, qs = _layered(q, "q", dt, L, (n, desc.n_q_heads, desc.head_dim), cur=cur)
+    o0, os_ = _layered(out, "out", dt, L, (n, desc.n_q_heads, desc.head_dim), cur=cur)
+    k0, ks = _layered(k_new, "k_new", dt, L, (n, desc.n_kv_heads, desc.head_dim), cur=cur)
+    v0, vs = _layered(v_new, "v_new", dt, L, (n, desc.n_kv_heads, desc.head_dim), cur=cur)
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur).value
+    tb = _dev(block_tables, "block_tables", t.int32, (n, mb), cur=cur).value
+    ln = _dev(context_lens, "context_lens", t.int32, (n,), cur=cur).value
+    wsp, wsb = (None, 0) if workspace is None else (_dev(workspace, "workspace", cur=cur).value,
                                                     workspace.numel() * workspace.element_size())
     fn, dref, sc, sh = lib().pkv_paged_decode_append_attention_ex, ctypes.byref(desc), float(scale), _raw_stream(stream)
 
@@ -442,17 +462,18 @@ def prefill_launcher(desc: CacheDesc, q, k_pool, v_pool, block_tables, context_l
     q/out [L, n_tokens, n_q, d] validated here once."""
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     L, n_tok = desc.n_layers, int(q.shape[1])
     if block_tables.dim() != 2:
         raise ValueError("block_tables must be [n_seqs, max_blocks]")
     n_seqs, mb = int(block_tables.shape[0]), int(block_tables.shape[1])
-    q0, qs = _layered(q, "q", dt, L, (n_tok, desc.n_q_heads, desc.head_dim))
-    o0, os_ = _layered(out, "out", dt, L, (n_tok, desc.n_q_heads, desc.head_dim))
-    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
-    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
-    tb = _dev(block_tables, "block_tables", t.int32, (n_seqs, mb)).value
-    ln = _dev(context_lens, "context_lens", t.int32, (n_seqs,)).value
-    qsd = _dev(query_start, "query_start", t.int32, (n_seqs + 1,)).value
+    q0, qs = _layered(q, "q", dt, L, (n_tok, desc.n_q_heads, desc.head_dim), cur=cur)
+    o0, os_ = _layered(out, "out", dt, L, (n_tok, desc.n_q_heads, desc.head_dim), cur=cur)
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur).value
+    tb = _dev(block_tables, "block_tables", t.int32, (n_seqs, mb), cur=cur).value
+    ln = _dev(context_lens, "context_lens", t.int32, (n_seqs,), cur=cur).value
+    qsd = _dev(query_start, "query_start", t.int32, (n_seqs + 1,), cur=cur).value
     fn, dref, sc, sh = lib().pkv_paged_prefill_attention_ex, ctypes.byref(desc), float(scale), _raw_stream(stream)
     mq = int(max_query_len)
 
@@ -468,12 +489,13 @@ def append_launcher(desc: CacheDesc, k, v, slot_mapping, k_pool, v_pool, stream=
     """launch(layer): pkv_kv_append of one layer, with k/v [L, n_tokens, n_kv, d] validated here once."""
     t = _torch()
     dt = torch_dtype(desc.dtype_name)
+    cur = _current_device()
     L, n_tok = desc.n_layers, int(k.shape[1])
-    k0, ks = _layered(k, "k", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim))
-    v0, vs = _layered(v, "v", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim))
-    sl = _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,)).value
-    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc)).value
-    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc)).value
+    k0, ks = _layered(k, "k", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim), cur=cur)
+    v0, vs = _layered(v, "v", dt, L, (n_tok, desc.n_kv_heads, desc.head_dim), cur=cur)
+    sl = _dev(slot_mapping, "slot_mapping", t.int64, (n_tok,), cur=cur).value
+    kp = _dev(k_pool, "k_pool", dt, pool_shape(desc), cur=cur).value
+    vp = _dev(v_pool, "v_pool", dt, pool_shape(desc), cur=cur).value
     fn, dref, sh = lib().pkv_kv_append, ctypes.byref(desc), _raw_stream(stream)
 
     def launch(layer: int) -> None:

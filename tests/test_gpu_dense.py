@@ -78,19 +78,24 @@ def test_dense_matches_oracle_and_paged_kernel(dtype, d, group):
 
 
 def test_dense_single_partition_and_overlap_flag_bit_identical():
-    """Short contexts (one partition) and a launch chained to the previous one give the same bits."""
+    """Short contexts over a grid that already fills the GPU (one partition per sequence, no
+    workspace) and a launch chained to the previous one give the same bits and the oracle's values."""
     import torch
-    q, kd, vd, lens = dense_case("f16", [5, 64, 100], 8, 8, 128, 128, seed=5)
+    lens = np.random.default_rng(5).integers(0, 129, size=80)
+    q, kd, vd, lens = dense_case("f16", lens, 8, 8, 128, 128, seed=5)
     desc = pkv.make_desc("f16", 1, 1, 8, 8, 128)
     q_t, k_t, v_t = to_torch(q, "f16"), to_torch(kd, "f16"), to_torch(vd, "f16")
     l_t = torch.from_numpy(lens).cuda()
-    assert pkv.pkv_decode_workspace_bytes(desc, 3, 8) == 0
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    single = pkv.pkv_decode_split_geometry(desc, 80, 8, sms)[1] == 1
+    ws = pkv.alloc_workspace(desc, 80, 8)
+    assert single == (ws is None)
     a = torch.empty_like(q_t)
     b = torch.empty_like(q_t)
-    pkv.pkv_dense_decode_attention(desc, 0, q_t, k_t, v_t, l_t, 0.1, a)
-    pkv.pkv_dense_decode_attention(desc, 0, q_t, k_t, v_t, l_t, 0.1, b, overlap_previous=True)
+    pkv.pkv_dense_decode_attention(desc, 0, q_t, k_t, v_t, l_t, 0.1, a, ws)
+    pkv.pkv_dense_decode_attention(desc, 0, q_t, k_t, v_t, l_t, 0.1, b, ws, overlap_previous=True)
     assert torch.equal(a, b)
-    tables = np.arange(3 * 8, dtype=np.int32).reshape(3, 8)
+    tables = np.arange(80 * 8, dtype=np.int32).reshape(80, 8)
     want = oracle.paged_decode("f16", q, as_pool(kd)[0], as_pool(vd)[0], tables, lens, 0.1)
     assert np.max(np.abs(as_f64(a) - want)) <= TOL["f16"]
     assert pkv.pkv_get_device_status() == 0
