@@ -501,6 +501,8 @@ def indirection(paged: dict, dense: dict) -> dict:
 # the target workloads measured beside the headline one in the default run (one line, keyed objects)
 SUB_CONFIGS = ("longdoc", "ragged", "prefix")
 DENSE_CONFIGS = ("gpt", "longdoc")  # the dense-cache comparison of the default run
+SHORT_STEPS = 200                   # timed steps of the one-layer workloads in the default run
+PREFIX_CHURN_STEPS = 256            # steps of the shared-prefix workload's churn log
 
 
 def run_gpu(args) -> dict | None:
@@ -518,14 +520,17 @@ def run_gpu(args) -> dict | None:
     cpu = ws == 1 and not args.no_cpu_baseline
     dense_for = set(DENSE_CONFIGS) if args.dense == "auto" else ({args.config} if args.dense == "on" else set())
 
-    def one(name, budget):
-        r = measure_decode(args, name, device, rank, ws, read_peak, cpu, budget)
-        if name in dense_for and args.placement == "shuffled":
+    def one_with(a, name, budget):
+        r = measure_decode(a, name, device, rank, ws, read_peak, cpu, budget)
+        if name in dense_for and a.placement == "shuffled":
             gc.collect()
             torch.cuda.empty_cache()
-            r["dense"] = measure_dense(args, name, device, rank, read_peak)
+            r["dense"] = measure_dense(a, name, device, rank, read_peak)
             r["indirection_overhead"] = indirection(r, r["dense"])
         return r
+
+    def one(name, budget):
+        return one_with(args, name, budget)
 
     res = one(args.config, args.cpu_budget)
     subs = {}
@@ -533,7 +538,16 @@ def run_gpu(args) -> dict | None:
         for name in SUB_CONFIGS:
             gc.collect()
             torch.cuda.empty_cache()
-            subs[name] = one(name, min(args.cpu_budget, 6.0))
+            # the one-layer workloads step in ~0.1-0.4 ms: time at least SHORT_STEPS of them, so that
+            # the timed region is not a few milliseconds that one host hiccup would distort
+            sub = argparse.Namespace(**vars(args))
+            if name == "ragged":
+                sub.steps = max(args.steps, SHORT_STEPS)
+            elif name == "prefix":  # its churn log has 256 steps: warm-up + value + roofline + e2e passes
+                sub.steps = max(args.steps, min(SHORT_STEPS, (PREFIX_CHURN_STEPS - args.warmup) // 3))
+            subs[name] = one_with(sub, name, min(args.cpu_budget, 6.0))
+            subs[name]["steps"] = sub.steps
+            subs[name]["warmup"] = sub.warmup
     if rank != 0:
         return None
     line = {

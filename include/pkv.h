@@ -114,26 +114,39 @@ uint64_t pkv_bytes_per_token(const pkv_cache_desc* desc);
 uint64_t pkv_pool_bytes(const pkv_cache_desc* desc);
 
 /*
- * Split-K geometry of paged decode attention on a device with sm_count multiprocessors, for
- * n_seqs sequences whose tables have max_blocks_per_seq columns (an interface helper; the pages
- * describe no kernel). A long context is cut into partitions of *blocks_per_partition table
- * entries (64, halved down to 4 while the grid n_seqs * n_kv_heads * *n_partitions would hold
- * fewer than 4 CTAs per multiprocessor), each computed by its own CTA and merged in the same
- * launch; *workspace_bytes receives the scratch those partials need (0 when *n_partitions is 1).
- * The decode calls use exactly this geometry with the current device's multiprocessor count.
- * Host-only arithmetic: needs no GPU. Output pointers may be NULL. PKV_ERR_INVALID_ARG when a
- * count is not positive; descriptor errors as pkv_validate_desc.
+ * Split-K geometry of paged decode attention (an interface helper; the pages describe no kernel)
+ * for n_seqs sequences whose tables have max_blocks_per_seq columns, on a device with sm_count
+ * multiprocessors that each hold ctas_per_sm CTAs of the decode kernel at once. A long context is
+ * cut into partitions of *blocks_per_partition table entries, each computed by its own CTA and
+ * merged in the same launch; *n_partitions = ceil(max_blocks_per_seq / *blocks_per_partition);
+ * *workspace_bytes receives the scratch those partials need (0 when *n_partitions is 1). With
+ * pairs = n_seqs * n_kv_heads and slots = sm_count * ctas_per_sm:
+ *   - one wave: if pairs < slots, parts = slots / pairs fills at least 3/4 of the slots and the
+ *     partitions ceil(max_blocks_per_seq / parts) are long (>= 64 entries; fp16 / bf16 pools,
+ *     whose kernel streams its table entries), that is the partition: the grid is one wave;
+ *   - otherwise 64 entries, halved (down to 4) while pairs * n_partitions < 4 * sm_count.
+ * The decode calls use exactly this geometry with the current device's facts
+ * (pkv_decode_ctas_per_sm). Host-only arithmetic: needs no GPU. Output pointers may be NULL.
+ * PKV_ERR_INVALID_ARG when a count is not positive; descriptor errors as pkv_validate_desc.
  */
 int pkv_decode_split_geometry(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq,
-                              int32_t sm_count, int32_t* blocks_per_partition, int32_t* n_partitions,
-                              size_t* workspace_bytes);
+                              int32_t sm_count, int32_t ctas_per_sm, int32_t* blocks_per_partition,
+                              int32_t* n_partitions, size_t* workspace_bytes);
+
+/*
+ * The current device's facts behind that geometry for pools of this descriptor: its multiprocessor
+ * count and how many CTAs of the decode kernel the descriptor selects one multiprocessor holds at
+ * once (the CUDA occupancy calculator: shared memory, registers, threads). Read once per device and
+ * kernel, then cached. Output pointers may be NULL. PKV_ERR_CUDA without a usable device.
+ */
+int pkv_decode_ctas_per_sm(const pkv_cache_desc* desc, int32_t* ctas_per_sm, int32_t* sm_count);
 
 /*
  * Scratch bytes pkv_paged_decode_attention needs on the current device for n_seqs sequences whose
  * tables have max_blocks_per_seq columns: split-K partial results plus one 8-byte arrival counter
  * per (sequence, KV head); 0 when no split is needed -- and also when the descriptor or a count is
  * invalid or no CUDA device can be queried. Equals pkv_decode_split_geometry's *workspace_bytes
- * for the current device's multiprocessor count (read once per device and cached).
+ * with the current device's pkv_decode_ctas_per_sm.
  */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t n_seqs, int32_t max_blocks_per_seq);
 

@@ -48,11 +48,10 @@ size_t layer_elems(const pkv_cache_desc* d) {
     return (size_t)d->num_blocks * d->n_kv_heads * d->block_size * d->head_dim;
 }
 
-size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int sm_count, int* bpp_out,
-                        int* n_parts_out, size_t* off_ml = nullptr, size_t* off_cnt = nullptr) {
-    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks, sm_count);
+// Workspace of a decode call with partitions of `bpp` table entries.
+size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int bpp, int* n_parts_out,
+                        size_t* off_ml = nullptr, size_t* off_cnt = nullptr) {
     const int n_parts = pkv::decode_partitions(max_blocks, bpp);
-    if (bpp_out) *bpp_out = bpp;
     if (n_parts_out) *n_parts_out = n_parts;
     size_t ml = 0, cnt = 0;
     const size_t bytes =
@@ -62,22 +61,44 @@ size_t decode_workspace(const pkv_cache_desc* d, int n_seqs, int max_blocks, int
     return bytes;
 }
 
+long long pool_rows(const pkv_cache_desc* d) { return (long long)d->num_blocks * d->n_kv_heads * d->block_size; }
+
 std::mutex g_sm_mu;
 int g_sm_count[64] = {};
+// CTAs per SM of each decode kernel: [device][dtype][head_dim 64/128/256][group 1/2/4/8][tensor-core path]
+int g_ctas_per_sm[64][3][3][4][2] = {};
+
+int dim_index(int head_dim) { return head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2; }
+int group_index(int g) { return g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : 3; }
 
 }  // namespace
 
 namespace pkv {
 
-// Blocks per partition: 64 (1,024 tokens) unless the grid would then hold fewer than ~4 CTAs per
-// SM, in which case partitions shrink (down to 4 blocks) to spread one long sequence over more
-// SMs. Depends only on the arguments, so the workspace query and the launch agree as long as both
-// pass the same SM count (both take it from current_sm_count).
-int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count) {
-    const long long target = 4LL * (sm_count > 0 ? sm_count : 1);
+// Blocks per partition.
+//  * One wave: when the grid's (sequence, KV head) pairs are fewer than the CTAs the GPU holds at
+//    once, each pair takes parts = slots / pairs CTAs; if that fills at least 3/4 of the slots with
+//    long partitions (>= 64 entries, which the tensor-core kernel streams), every context is cut
+//    into `parts` equal partitions and the launch is one wave of equal CTAs: no CTA starts after
+//    another has finished, so no SM idles through a tail while the last ones run (long documents:
+//    10 sequences x 4 KV heads spread over 11 CTAs each instead of 2.9 waves of 33).
+//  * Otherwise 64 entries (1,024 tokens), halved (down to 4) while the grid would hold fewer than
+//    ~4 CTAs per SM, to spread a few long sequences over more SMs.
+// Depends only on the arguments, so the workspace query and the launch agree as long as both pass
+// the same device facts (both take them from decode_geometry).
+int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count, int ctas_per_sm, int max_bpp) {
+    const long long pairs = (long long)n_seqs * n_kv;
+    const long long sms = sm_count > 0 ? sm_count : 1;
+    const long long slots = sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    if (pairs > 0 && pairs < slots) {
+        const long long parts = slots / pairs;
+        const long long bpp1 = (max_blocks + parts - 1) / parts;
+        if (4 * pairs * parts >= 3 * slots && bpp1 >= kMaxBpp && bpp1 <= max_bpp) return (int)bpp1;
+    }
+    const long long target = 4LL * sms;
     int bpp = kMaxBpp;
-    while (bpp > 4 && (long long)n_seqs * n_kv * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
-    return bpp;
+    while (bpp > 4 && pairs * ((max_blocks + bpp - 1) / bpp) < target) bpp /= 2;
+    return bpp < max_bpp ? bpp : max_bpp;
 }
 
 // SMs of the current device (cudaDevAttrMultiProcessorCount), read once per device.
@@ -95,6 +116,46 @@ cudaError_t current_sm_count(int* out) {
         g_sm_count[dev] = n;
     }
     *out = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+cudaError_t decode_ctas_per_sm(int dtype, int head_dim, int group, long long rows, int* out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64 || dtype < 0 || dtype > 2) return cudaErrorInvalidValue;
+    int& slot = g_ctas_per_sm[dev][dtype][dim_index(head_dim)][group_index(group)][decode_uses_mma(dtype, group, rows)];
+    {
+        std::lock_guard<std::mutex> lock(g_sm_mu);
+        if (slot > 0) {
+            *out = slot;
+            return cudaSuccess;
+        }
+    }
+    int n = 0;
+    switch (dtype) {
+    case PKV_F32: err = decode_ctas_per_sm_f32(head_dim, group, rows, &n); break;
+    case PKV_F16: err = decode_ctas_per_sm_f16(head_dim, group, rows, &n); break;
+    default: err = decode_ctas_per_sm_bf16(head_dim, group, rows, &n); break;
+    }
+    if (err != cudaSuccess) return err;
+    if (n <= 0) return cudaErrorInvalidConfiguration;  // the kernel does not fit on an SM
+    std::lock_guard<std::mutex> lock(g_sm_mu);
+    slot = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+cudaError_t decode_geometry(const pkv_cache_desc* d, long long rows, int n_seqs, int max_blocks, int* bpp,
+                            int* n_parts) {
+    int sms = 0, per_sm = 0;
+    const int group = d->n_q_heads / d->n_kv_heads;
+    cudaError_t err = current_sm_count(&sms);
+    if (err == cudaSuccess) err = decode_ctas_per_sm(d->dtype, d->head_dim, group, rows, &per_sm);
+    if (err != cudaSuccess) return err;
+    *bpp = decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks, sms, per_sm,
+                                       decode_max_bpp(d->dtype, group, rows));
+    *n_parts = decode_partitions(max_blocks, *bpp);
     return cudaSuccess;
 }
 
@@ -162,27 +223,45 @@ uint64_t pkv_pool_bytes(const pkv_cache_desc* d) {
 }
 
 int pkv_decode_split_geometry(const pkv_cache_desc* d, int32_t n_seqs, int32_t max_blocks_per_seq,
-                              int32_t sm_count, int32_t* blocks_per_partition, int32_t* n_partitions,
-                              size_t* workspace_bytes) {
+                              int32_t sm_count, int32_t ctas_per_sm, int32_t* blocks_per_partition,
+                              int32_t* n_partitions, size_t* workspace_bytes) {
     int rc = pkv_validate_desc(d);
     if (rc != PKV_OK) return rc;
-    if (n_seqs <= 0 || max_blocks_per_seq <= 0 || sm_count <= 0) return PKV_ERR_INVALID_ARG;
-    int bpp = 0, n_parts = 0;
-    const size_t bytes = decode_workspace(d, n_seqs, max_blocks_per_seq, sm_count, &bpp, &n_parts);
+    if (n_seqs <= 0 || max_blocks_per_seq <= 0 || sm_count <= 0 || ctas_per_sm <= 0) return PKV_ERR_INVALID_ARG;
+    const int group = d->n_q_heads / d->n_kv_heads;
+    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks_per_seq, sm_count, ctas_per_sm,
+                                                     pkv::decode_max_bpp(d->dtype, group, pool_rows(d)));
+    int n_parts = 0;
+    const size_t bytes = decode_workspace(d, n_seqs, max_blocks_per_seq, bpp, &n_parts);
     if (blocks_per_partition) *blocks_per_partition = bpp;
     if (n_partitions) *n_partitions = n_parts;
     if (workspace_bytes) *workspace_bytes = bytes;
     return PKV_OK;
 }
 
+int pkv_decode_ctas_per_sm(const pkv_cache_desc* d, int32_t* ctas_per_sm, int32_t* sm_count) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    int sms = 0, per_sm = 0;
+    if (pkv::current_sm_count(&sms) != cudaSuccess ||
+        pkv::decode_ctas_per_sm(d->dtype, d->head_dim, d->n_q_heads / d->n_kv_heads, pool_rows(d), &per_sm) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    if (ctas_per_sm) *ctas_per_sm = per_sm;
+    if (sm_count) *sm_count = sms;
+    return PKV_OK;
+}
+
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* d, int32_t n_seqs, int32_t max_blocks_per_seq) {
     if (pkv_validate_desc(d) != PKV_OK || n_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
-    int sms = 0;
-    if (pkv::current_sm_count(&sms) != cudaSuccess) {
+    int bpp = 0, n_parts = 0;
+    if (pkv::decode_geometry(d, pool_rows(d), n_seqs, max_blocks_per_seq, &bpp, &n_parts) != cudaSuccess) {
         cudaGetLastError();  // no usable device: report nothing rather than a guess
         return 0;
     }
-    return decode_workspace(d, n_seqs, max_blocks_per_seq, sms, nullptr, nullptr);
+    return decode_workspace(d, n_seqs, max_blocks_per_seq, bpp, nullptr);
 }
 
 int pkv_kv_append(const pkv_cache_desc* d, int32_t layer, const void* k, const void* v, const int64_t* slot_mapping,
@@ -229,17 +308,17 @@ static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, c
     if (!q || !k_pool || !v_pool || (!block_tables && !dense) || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
     if ((k_new || v_new) && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
-    int sms = 0;
-    if (pkv::current_sm_count(&sms) != cudaSuccess) return PKV_ERR_CUDA;
-    int bpp = 0, n_parts = 0;
-    size_t off_ml = 0, off_cnt = 0;
-    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, sms, &bpp, &n_parts, &off_ml, &off_cnt);
-    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
-
-    pkv::DecodeArgs a;
     // a dense layer holds n_seqs * max_blocks 16-row chunks per KV head: the pool geometry with
     // num_blocks = n_seqs * max_blocks
     const int num_blocks = dense ? n_seqs * max_blocks_per_seq : d->num_blocks;
+    const long long rows = (long long)num_blocks * d->n_kv_heads * d->block_size;
+    int bpp = 0, n_parts = 0;
+    if (pkv::decode_geometry(d, rows, n_seqs, max_blocks_per_seq, &bpp, &n_parts) != cudaSuccess) return PKV_ERR_CUDA;
+    size_t off_ml = 0, off_cnt = 0;
+    const size_t need = decode_workspace(d, n_seqs, max_blocks_per_seq, bpp, &n_parts, &off_ml, &off_cnt);
+    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
+
+    pkv::DecodeArgs a;
     const size_t layer_bytes =
         (size_t)num_blocks * d->n_kv_heads * d->block_size * d->head_dim * elem_bytes(d->dtype);
     a.q = q;

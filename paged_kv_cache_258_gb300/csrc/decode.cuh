@@ -550,25 +550,61 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeArgs 
                                                reinterpret_cast<float*>(smem + S::MERGE));
 }
 
-template <typename T, int D, int G>
-cudaError_t launch_decode_tpl(const DecodeArgs& a, cudaStream_t stream, int* n_launches) {
-    constexpr int NW = DecodeTuning<T, D, G>::NW;
-    constexpr int ST = DecodeTuning<T, D, G>::ST;
-    constexpr size_t smem = DecodeSmem<T, D, G, NW, ST>::TOTAL;
-    auto kern = paged_decode_kernel<T, D, G, NW, ST>;
+// Lets `kern` use `smem` bytes of dynamic shared memory on the current device (once per device; a
+// benign race, the call is idempotent).
+template <typename K>
+cudaError_t allow_dynamic_smem(K kern, size_t smem, unsigned long long* done) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    static unsigned long long attr_done = 0;  // one bit per device (benign race: idempotent)
-    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    if (dev < 64 && !(__atomic_load_n(done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
+        __atomic_fetch_or(done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
+    return cudaSuccess;
+}
+
+template <typename T, int D, int G>
+struct DecodeKernel {
+    static constexpr int NW = DecodeTuning<T, D, G>::NW;
+    static constexpr int ST = DecodeTuning<T, D, G>::ST;
+    static constexpr size_t smem = DecodeSmem<T, D, G, NW, ST>::TOTAL;
+    static unsigned long long attr_done;
+    static cudaError_t prepare() { return allow_dynamic_smem(paged_decode_kernel<T, D, G, NW, ST>, smem, &attr_done); }
+    // CTAs of this kernel one SM holds at once (shared memory, registers, threads)
+    static cudaError_t ctas_per_sm(int* out) {
+        cudaError_t err = prepare();
+        if (err != cudaSuccess) return err;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, paged_decode_kernel<T, D, G, NW, ST>, NW * 32, smem);
+    }
+};
+template <typename T, int D, int G>
+unsigned long long DecodeKernel<T, D, G>::attr_done = 0;
+
+template <typename T, int D, int G>
+cudaError_t launch_decode_tpl(const DecodeArgs& a, cudaStream_t stream, int* n_launches) {
+    using K = DecodeKernel<T, D, G>;
+    constexpr int NW = K::NW;
+    constexpr size_t smem = K::smem;
+    auto kern = paged_decode_kernel<T, D, G, NW, K::ST>;
+    cudaError_t err = K::prepare();
+    if (err != cudaSuccess) return err;
     dim3 grid(a.n_parts, a.n_kv, a.n_seqs);
     kern<<<grid, NW * 32, smem, stream>>>(a);
     if (n_launches) *n_launches = 1;
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t decode_ctas_per_sm_dtype(int head_dim, int group, int* out) {
+#define PKV_CASE(DD, GG) \
+    if (head_dim == DD && group == GG) return DecodeKernel<T, DD, GG>::ctas_per_sm(out);
+    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+    PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+    PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
+#undef PKV_CASE
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>

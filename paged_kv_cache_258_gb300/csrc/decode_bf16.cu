@@ -16,4 +16,9 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const DecodeArgs& a, cud
     return launch_decode_dtype<__nv_bfloat16>(head_dim, group, a, stream, n_launches);
 }
 
+cudaError_t decode_ctas_per_sm_bf16(int head_dim, int group, long long rows, int* out) {
+    if (decode_uses_mma(PKV_BF16, group, rows)) return decode_mma_ctas_per_sm_dtype<__nv_bfloat16>(head_dim, group, out);
+    return decode_ctas_per_sm_dtype<__nv_bfloat16>(head_dim, group, out);
+}
+
 }  // namespace pkv

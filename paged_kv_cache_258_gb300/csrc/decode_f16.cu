@@ -16,4 +16,9 @@ cudaError_t launch_decode_f16(int head_dim, int group, const DecodeArgs& a, cuda
     return launch_decode_dtype<__half>(head_dim, group, a, stream, n_launches);
 }
 
+cudaError_t decode_ctas_per_sm_f16(int head_dim, int group, long long rows, int* out) {
+    if (decode_uses_mma(PKV_F16, group, rows)) return decode_mma_ctas_per_sm_dtype<__half>(head_dim, group, out);
+    return decode_ctas_per_sm_dtype<__half>(head_dim, group, out);
+}
+
 }  // namespace pkv

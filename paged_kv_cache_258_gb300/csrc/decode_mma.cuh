@@ -112,8 +112,7 @@ struct MmaSmem {
     static constexpr size_t STAGES = (size_t)NW * ST * 2 * TILE;     // 1024-aligned base
     static constexpr size_t BARS = STAGES;                           // uint64 [NW][ST][K, V]
     static constexpr size_t PHYS = BARS + (size_t)NW * ST * 16;     // int [NW][ST]
-    static constexpr size_t TAB = PHYS + (size_t)NW * ST * 4;       // int [NW][kMaxBpp/NW]: block ids
-    static constexpr size_t ML = (TAB + (size_t)kMaxBpp * 4 + 15) / 16 * 16;  // float [NW][8][2]
+    static constexpr size_t ML = (PHYS + (size_t)NW * ST * 4 + 15) / 16 * 16;  // float [NW][8][2]
     static constexpr size_t TOTAL = ML + (size_t)NW * 8 * 2 * 4;
     static constexpr size_t ALLOC = TOTAL + 1024;                     // room to align the base
     static constexpr size_t MERGE = (size_t)NW * 8 * D * 4;          // merge scratch, after the combine buffer
@@ -150,15 +149,18 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     // SMs this grid's tail leaves idle. Without such a launch this is a no-op.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // This warp's table entries of the partition (blocks p*bpp + warp + k*NW, k < kMaxBpp/NW <= 32),
-    // loaded before the context length is known so the two global reads overlap; entries past the
-    // sequence's last block are read (inside the table row) but never used.
-    static_assert(kMaxBpp / NW <= 32, "one table entry per lane");
-    int tab_pre = -1;
-    {
-        const int idx = p * a.bpp + warp + lane * NW;
-        if (lane < kMaxBpp / NW && idx < a.max_blocks) tab_pre = walk_entry(a, s, idx);
-    }
+    // This warp's blocks of the partition are p*bpp + warp + k*NW (k < nk). Their table entries live
+    // in registers, 32 per chunk (lane l holds entry 32c + l of chunk c): chunk 0 is read before the
+    // context length is known, so the two global reads overlap, and each later chunk one chunk ahead
+    // of its first use. Entries past the sequence's last block are read (inside the table row) but
+    // never used.
+    auto load_chunk = [&](int c) -> int {
+        const long long kk = (long long)c * 32 + lane;
+        const long long idx = (long long)p * a.bpp + warp + kk * NW;
+        return kk * NW + warp < a.bpp && idx < a.max_blocks ? walk_entry(a, s, (int)idx) : -1;
+    };
+    int tab_lo = load_chunk(0);                        // entries of chunk c_lo
+    int tab_hi = a.bpp > 32 * NW ? load_chunk(1) : -1;  // entries of chunk c_lo + 1
     int ctx = a.lens[s];
     const int cap = a.max_blocks * kBlock;
     if (ctx < 0 || ctx > cap) {
@@ -189,15 +191,21 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     int* wphys = s_phys + warp * ST;
     const uint32_t wstage = smem_addr(smem) + (uint32_t)(warp * ST) * 2 * TILE;
     unsigned char* wstage_ptr = smem + (size_t)warp * ST * 2 * TILE;
-    static_assert(kMaxBpp % NW == 0, "each warp stages kMaxBpp / NW table entries");
-    int* wtab = reinterpret_cast<int*>(smem + S::TAB) + warp * (kMaxBpp / NW);
     const int nk = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
     const uint64_t policy = l2_evict_first_policy();
 
+    // Every lane: the physical block of this warp's k-th block, for k = 0, 1, 2, ... in order (each
+    // exactly once); entering chunk c moves to it and starts the read of chunk c + 1.
+    auto entry = [&](int k) -> int {
+        if ((k & 31) == 0 && k > 0) {
+            tab_lo = tab_hi;
+            tab_hi = load_chunk((k >> 5) + 1);
+        }
+        return __shfl_sync(0xffffffffu, tab_lo, k & 31);
+    };
     // lane 0: start the copy of the K (v = 0) or V (v = 1) tile of this warp's k-th block
-    auto issue = [&](int k, int v) {
+    auto issue = [&](int k, int v, int phys) {
         const int st = k % ST;
-        const int phys = wtab[k];
         const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
         uint64_t* bar = &wbars[st * 2 + v];
         if (v == 0) wphys[st] = ok ? phys : -1;
@@ -216,14 +224,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     auto drain = [&](int k0, int k1, int v) {
         for (int kk = k0; kk < k1 && kk < nk; ++kk) mbar_wait_bounded(&wbars[(kk % ST) * 2 + v], (uint32_t)(kk / ST) & 1u);
     };
-    // this warp's table entries (blocks warp, warp+NW, ...) staged once, so issuing a copy never
-    // waits on a global read of the table
-    if (lane < nk) wtab[lane] = tab_pre;
-    __syncwarp();
-    if (lane == 0) {
-        for (int k = 0; k < ST && k < nk; ++k) {
-            issue(k, 0);
-            issue(k, 1);
+    for (int k = 0; k < ST && k < nk; ++k) {
+        const int phys = entry(k);
+        if (lane == 0) {
+            issue(k, 0, phys);
+            issue(k, 1, phys);
         }
     }
 
@@ -261,6 +266,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
     for (int k = 0; k < nk; ++k) {
         const int st = k % ST;
         const uint32_t par = (uint32_t)(k / ST) & 1u;
+        const int phys_next = k + ST < nk ? entry(k + ST) : -1;  // the block whose copies go next
         if (!mbar_wait_bounded(&wbars[st * 2], par)) {
             if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
             drain(k, k + ST, 0);  // K tiles of blocks k .. k+ST-1 may be in flight
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
         __syncwarp();  // the K tile has been read by every lane
         if (lane == 0 && k + ST < nk) {
             fence_proxy_async_smem();
-            issue(k + ST, 0);
+            issue(k + ST, 0, phys_next);
         }
         if (!mbar_wait_bounded(&wbars[st * 2 + 1], par)) {
             if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_mma_kernel(const DecodeA
         __syncwarp();  // the V tile has been read by every lane
         if (lane == 0 && k + ST < nk) {
             fence_proxy_async_smem();
-            issue(k + ST, 1);
+            issue(k + ST, 1, phys_next);
         }
     }
 
@@ -434,21 +440,34 @@ struct MmaTuning {
 };
 
 template <typename T, int D, int G>
+struct DecodeMmaKernel {
+    static constexpr int NW = MmaTuning<T, D, G>::NW;
+    static constexpr int ST = MmaTuning<T, D, G>::ST;
+    static constexpr size_t smem = MmaSmem<D, NW, ST>::ALLOC;
+    static unsigned long long attr_done;
+    static cudaError_t prepare() {
+        return allow_dynamic_smem(paged_decode_mma_kernel<T, D, G, NW, ST>, smem, &attr_done);
+    }
+    // CTAs of this kernel one SM holds at once (shared memory, registers, threads)
+    static cudaError_t ctas_per_sm(int* out) {
+        cudaError_t err = prepare();
+        if (err != cudaSuccess) return err;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, paged_decode_mma_kernel<T, D, G, NW, ST>, NW * 32,
+                                                             smem);
+    }
+};
+template <typename T, int D, int G>
+unsigned long long DecodeMmaKernel<T, D, G>::attr_done = 0;
+
+template <typename T, int D, int G>
 cudaError_t launch_decode_mma_tpl(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                   cudaStream_t stream, int* n_launches) {
-    constexpr int NW = MmaTuning<T, D, G>::NW;
-    constexpr int ST = MmaTuning<T, D, G>::ST;
-    constexpr size_t smem = MmaSmem<D, NW, ST>::ALLOC;
-    auto kern = paged_decode_mma_kernel<T, D, G, NW, ST>;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    using K = DecodeMmaKernel<T, D, G>;
+    constexpr int NW = K::NW;
+    constexpr size_t smem = K::smem;
+    auto kern = paged_decode_mma_kernel<T, D, G, NW, K::ST>;
+    cudaError_t err = K::prepare();
     if (err != cudaSuccess) return err;
-    static unsigned long long attr_done = 0;
-    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_parts, a.n_kv, a.n_seqs);
     cfg.blockDim = dim3(NW * 32, 1, 1);
@@ -463,6 +482,17 @@ cudaError_t launch_decode_mma_tpl(const DecodeArgs& a, const CUtensorMap& tk, co
     if (err != cudaSuccess) return err;
     if (n_launches) *n_launches = 1;
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t decode_mma_ctas_per_sm_dtype(int head_dim, int group, int* out) {
+#define PKV_CASE(DD, GG) \
+    if (head_dim == DD && group == GG) return DecodeMmaKernel<T, DD, GG>::ctas_per_sm(out);
+    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+    PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+    PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
+#undef PKV_CASE
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>

@@ -63,10 +63,10 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
 
     // Same partition geometry, hence the same scratch need, as pkv_paged_decode_attention.
-    int sms = 0;
-    if (pkv::current_sm_count(&sms) != cudaSuccess) return PKV_ERR_CUDA;
-    const int bpp = pkv::decode_blocks_per_partition(n_seqs, d->n_kv_heads, max_blocks_per_seq, sms);
-    const int n_parts = pkv::decode_partitions(max_blocks_per_seq, bpp);
+    int bpp = 0, n_parts = 0;
+    if (pkv::decode_geometry(d, (long long)d->num_blocks * d->n_kv_heads * d->block_size, n_seqs, max_blocks_per_seq,
+                             &bpp, &n_parts) != cudaSuccess)
+        return PKV_ERR_CUDA;
     size_t off_ml = 0, off_cnt = 0;
     const size_t need =
         pkv::decode_workspace_layout(n_seqs, d->n_q_heads, d->n_kv_heads, d->head_dim, n_parts, &off_ml, &off_cnt);

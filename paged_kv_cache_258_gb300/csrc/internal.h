@@ -88,10 +88,21 @@ struct CopyArgs {
     size_t layer_bytes;     // num_blocks * block_bytes
 };
 
-// Partition geometry shared by the workspace query and the launch; sm_count is the device's
-// multiprocessor count (current_sm_count), so that the split fills the part it runs on.
-int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count);
+// Partition geometry shared by the workspace query and the launch. sm_count is the device's
+// multiprocessor count, ctas_per_sm the number of CTAs of the chosen decode kernel one SM holds at
+// once, max_bpp the largest partition that kernel takes (decode_max_bpp).
+int decode_blocks_per_partition(int n_seqs, int n_kv, int max_blocks, int sm_count, int ctas_per_sm, int max_bpp);
 cudaError_t current_sm_count(int* out);
+// CTAs per SM of the decode kernel a call of this shape runs (pool rows decide the kernel, as in
+// decode_uses_mma), measured by the occupancy calculator on the current device.
+cudaError_t decode_ctas_per_sm(int dtype, int head_dim, int group, long long rows, int* out);
+cudaError_t decode_ctas_per_sm_f32(int head_dim, int group, long long rows, int* out);
+cudaError_t decode_ctas_per_sm_f16(int head_dim, int group, long long rows, int* out);
+cudaError_t decode_ctas_per_sm_bf16(int head_dim, int group, long long rows, int* out);
+// The geometry of a decode call on the current device (SM count and occupancy read once per device
+// and kernel, then cached): blocks per partition and partitions per sequence.
+cudaError_t decode_geometry(const pkv_cache_desc* d, long long rows, int n_seqs, int max_blocks, int* bpp,
+                            int* n_parts);
 inline int decode_partitions(int max_blocks, int bpp) { return (max_blocks + bpp - 1) / bpp; }
 
 // Split-K workspace layout (0 bytes when n_parts <= 1): fp32 partial outputs
@@ -129,6 +140,13 @@ cudaError_t launch_upload_metadata(void* dst, const void* src, size_t bytes, cud
 constexpr int kMmaMinGroup = 1;
 inline bool decode_uses_mma(int dtype, int group, long long rows) {
     return dtype != PKV_F32 && group >= kMmaMinGroup && rows < (1LL << 31);
+}
+// Largest partition (table entries per CTA) of the chosen kernel: the CUDA-core kernel stages a
+// partition's entries in shared memory (kMaxBpp of them); the tensor-core kernel streams them
+// through registers and takes any length.
+constexpr int kMaxBppStreamed = 1 << 24;
+inline int decode_max_bpp(int dtype, int group, long long rows) {
+    return decode_uses_mma(dtype, group, rows) ? kMaxBppStreamed : kMaxBpp;
 }
 
 // Status of a launcher's result: a pool address the tensor maps refused (not device memory of the

@@ -175,6 +175,9 @@ class DecodeBatch:
         self.total_cow = 0
         self.manager_s = 0.0       # host time in the block manager (append + pack), waits excluded
         self.steps_planned = 0
+        # validated per-layer launchers, one per device metadata image, for the step tensors they
+        # were built for (kept alive here, so an identity match means the same tensors)
+        self._launchers = [None, None]
 
     def _views(self, buf):
         n, mb = self.n, self.max_blocks
@@ -238,9 +241,17 @@ class DecodeBatch:
         self.d_slots, self.d_tables, self.d_lens, self.d_pairs = dv["slots"], dv["tables"], dv["lens"], dv["pairs"]
         if st["npairs"]:
             pkv.pkv_copy_blocks(d, c.k_pool, c.v_pool, self.d_pairs[: st["npairs"]], stream=self.stream)
-        if self.fused:  # the step's tensors checked once; each layer is then one C call
-            launch = pkv.decode_append_launcher(d, q, k_new, v_new, c.k_pool, c.v_pool, self.d_tables, self.d_lens,
-                                                scale, out, self.workspace, stream=self.stream)
+        if self.fused:  # the step's tensors checked once (and again only when they change); each
+            # layer is then one C call
+            key = (q, k_new, v_new, out, float(scale))
+            hit = self._launchers[st["buf"]]
+            if hit is not None and len(hit[0]) == len(key) and all(a is b for a, b in zip(hit[0][:4], key[:4])) \
+                    and hit[0][4] == key[4]:
+                launch = hit[1]
+            else:
+                launch = pkv.decode_append_launcher(d, q, k_new, v_new, c.k_pool, c.v_pool, self.d_tables,
+                                                    self.d_lens, scale, out, self.workspace, stream=self.stream)
+                self._launchers[st["buf"]] = (key, launch)
         for layer in range(d.n_layers):
             if on_decode is not None:
                 on_decode(layer, "pre")  # before anything of this layer is launched

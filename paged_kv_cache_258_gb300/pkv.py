@@ -69,8 +69,9 @@ def lib():
         "pkv_bytes_per_token": (c_u64, [dp]),
         "pkv_pool_bytes": (c_u64, [dp]),
         "pkv_decode_workspace_bytes": (c_sz, [dp, c_i32, c_i32]),
-        "pkv_decode_split_geometry": (ctypes.c_int, [dp, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
+        "pkv_decode_split_geometry": (ctypes.c_int, [dp, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                                      ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]),
+        "pkv_decode_ctas_per_sm": (ctypes.c_int, [dp, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]),
         "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
         "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
                                                       vp, vp, c_sz, vp]),
@@ -205,13 +206,24 @@ def pkv_decode_workspace_bytes(desc: CacheDesc, n_seqs: int, max_blocks_per_seq:
     return int(lib().pkv_decode_workspace_bytes(ctypes.byref(desc), int(n_seqs), int(max_blocks_per_seq)))
 
 
-def pkv_decode_split_geometry(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, sm_count: int):
-    """(blocks per partition, partitions, workspace bytes) of decode on a part with sm_count SMs."""
+def pkv_decode_split_geometry(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: int, sm_count: int,
+                              ctas_per_sm: int):
+    """(blocks per partition, partitions, workspace bytes) of decode on a part with sm_count SMs that
+    each hold ctas_per_sm decode CTAs."""
     bpp, nparts, nbytes = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_size_t(0)
     _check(lib().pkv_decode_split_geometry(ctypes.byref(desc), int(n_seqs), int(max_blocks_per_seq), int(sm_count),
-                                           ctypes.byref(bpp), ctypes.byref(nparts), ctypes.byref(nbytes)),
+                                           int(ctas_per_sm), ctypes.byref(bpp), ctypes.byref(nparts),
+                                           ctypes.byref(nbytes)),
            "pkv_decode_split_geometry")
     return int(bpp.value), int(nparts.value), int(nbytes.value)
+
+
+def pkv_decode_ctas_per_sm(desc: CacheDesc):
+    """(decode CTAs per SM for this descriptor, SM count) on the current device."""
+    per_sm, sms = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().pkv_decode_ctas_per_sm(ctypes.byref(desc), ctypes.byref(per_sm), ctypes.byref(sms)),
+           "pkv_decode_ctas_per_sm")
+    return int(per_sm.value), int(sms.value)
 
 
 def pkv_kv_append(desc: CacheDesc, layer: int, k, v, slot_mapping, k_pool, v_pool, stream=None) -> None:

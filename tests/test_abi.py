@@ -58,8 +58,8 @@ def test_validate_desc(kw, want):
     assert pkv.pkv_validate_desc(pkv.make_desc(**kw)) == want
 
 
-def _ws(desc, n_seqs, max_blocks, sms=152):
-    return pkv.pkv_decode_split_geometry(desc, n_seqs, max_blocks, sms)[2]
+def _ws(desc, n_seqs, max_blocks, sms=152, per_sm=3):
+    return pkv.pkv_decode_split_geometry(desc, n_seqs, max_blocks, sms, per_sm)[2]
 
 
 def test_workspace_only_when_split():
@@ -68,29 +68,50 @@ def test_workspace_only_when_split():
     n = _ws(d, 64, 129)
     assert n == 64 * 32 * 3 * (128 + 2) * 4 + 64 * 32 * 8          # 129 blocks -> 3 partitions of 64
     d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)
-    assert _ws(d4, 10, 2048) == 10 * 16 * 32 * (256 + 2) * 4 + 10 * 4 * 8
+    # 40 (sequence, KV head) pairs over 456 slots: one wave of 11 partitions of 187 blocks each
+    assert _ws(d4, 10, 2048) == 10 * 16 * 11 * (256 + 2) * 4 + 10 * 4 * 8
     with pytest.raises(pkv.PkvError):
-        pkv.pkv_decode_split_geometry(d, 0, 10, 152)
+        pkv.pkv_decode_split_geometry(d, 0, 10, 152, 3)
     with pytest.raises(pkv.PkvError):
-        pkv.pkv_decode_split_geometry(d, 4, 10, 0)
+        pkv.pkv_decode_split_geometry(d, 4, 10, 0, 3)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_decode_split_geometry(d, 4, 10, 152, 0)
     assert pkv.pkv_decode_workspace_bytes(d, 0, 10) == 0
 
 
-def test_split_geometry_follows_the_sm_count():
-    """Partitions shrink until the grid holds at least 4 CTAs per SM of the part it runs on."""
-    d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)      # 10 sequences x 4 KV heads x 2,048 blocks
-    for sms, bpp in [(152, 64), (76, 64), (20, 64), (304, 64), (400, 32), (1000, 16), (4000, 4), (10 ** 6, 4)]:
-        got_bpp, n_parts, nbytes = pkv.pkv_decode_split_geometry(d4, 10, 2048, sms)
-        assert got_bpp == bpp, sms
-        assert n_parts == -(-2048 // bpp)
-        assert 10 * 4 * n_parts >= 4 * sms or bpp == 4      # the target, unless partitions are minimal
-        assert nbytes == 10 * 16 * n_parts * (256 + 2) * 4 + 10 * 4 * 8
-    d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)          # gpt-like: 64 x 32 CTAs already fill 152 SMs
-    assert pkv.pkv_decode_split_geometry(d, 64, 129, 152)[:2] == (64, 3)
-    assert pkv.pkv_decode_split_geometry(d, 64, 129, 2048)[:2] == (32, 5)
-    # a single sequence and head is spread as far as 4-block partitions allow, whatever the part
+@pytest.mark.parametrize("sms,per_sm,bpp,n_parts", [
+    (152, 3, 187, 11),     # 440 of 456 slots: one wave of equal CTAs
+    (76, 3, 410, 5),       # 200 of 228
+    (152, 2, 293, 7),      # 280 of 304
+    (20, 1, 64, 32),       # more pairs than slots: several waves of 64-block partitions
+    (1000, 3, 16, 128),    # the one-wave partitions would be short (28 blocks): ~4 CTAs per SM instead
+])
+def test_split_geometry_follows_the_device(sms, per_sm, bpp, n_parts):
+    """10 sequences x 4 KV heads x 2,048 blocks (the long-document shape) on parts of other sizes."""
+    d4 = pkv.make_desc("bf16", 16, 30000, 16, 4, 256)
+    got_bpp, got_parts, nbytes = pkv.pkv_decode_split_geometry(d4, 10, 2048, sms, per_sm)
+    assert (got_bpp, got_parts) == (bpp, n_parts)
+    assert got_parts == -(-2048 // got_bpp)
+    assert nbytes == 10 * 16 * n_parts * (256 + 2) * 4 + 10 * 4 * 8
+
+
+def test_split_geometry_rules():
+    # fp32 pools run the CUDA-core kernel, whose partitions stop at 64 entries: no one-wave split
+    d32 = pkv.make_desc("f32", 16, 30000, 16, 4, 256)
+    assert pkv.pkv_decode_split_geometry(d32, 10, 2048, 152, 3)[:2] == (64, 32)
+    # as many pairs as slots or more: 64-entry partitions (the GPT-style batch: 64 x 32 pairs)
+    d = pkv.make_desc("f16", 1, 4096, 32, 32, 128)
+    assert pkv.pkv_decode_split_geometry(d, 64, 129, 152, 3)[:2] == (64, 3)
+    # one wave would leave over a quarter of the slots empty (256 pairs, 1 CTA each): 64 entries
+    d_gqa = pkv.make_desc("f16", 1, 4096, 32, 4, 128)
+    assert pkv.pkv_decode_split_geometry(d_gqa, 64, 140, 152, 3)[:2] == (64, 3)
+    # a single sequence and head is spread as far as 4-block partitions allow
     one = pkv.make_desc("f16", 1, 4096, 1, 1, 128)
-    assert pkv.pkv_decode_split_geometry(one, 1, 128, 8)[:2] == (4, 32)
+    assert pkv.pkv_decode_split_geometry(one, 1, 128, 8, 3)[:2] == (4, 32)
+    # a growing slot count never shrinks a one-wave partition below 64 entries
+    for sms in range(100, 400, 7):
+        b, n, _ = pkv.pkv_decode_split_geometry(pkv.make_desc("bf16", 1, 30000, 16, 4, 256), 10, 2048, sms, 3)
+        assert b >= 4 and n == -(-2048 // b) and (b >= 64 or 40 * n >= 4 * sms)
 
 
 def test_device_calls_reject_bad_arguments_before_launch():

@@ -262,8 +262,9 @@ def test_bounded_wait_gives_up_and_context_stays_usable():
 
 
 def test_workspace_query_and_launch_use_the_devices_sm_count():
-    """The workspace query reads this device's SM count; a workspace of exactly that size is
-    accepted and one byte less is refused before launch, so query and launch agree."""
+    """The workspace query reads this device's SM count and the decode kernel's occupancy; a
+    workspace of exactly that size is accepted and one byte less is refused before launch, so query
+    and launch agree."""
     import ctypes
 
     import torch
@@ -271,9 +272,11 @@ def test_workspace_query_and_launch_use_the_devices_sm_count():
     lens = [3000, 17, 900]
     q, kp, vp, tables, lens, nb = paged_case("bf16", lens, 16, 4, 256, seed=77)
     desc = pkv.make_desc("bf16", 1, nb, 16, 4, 256)
+    per_sm, got_sms = pkv.pkv_decode_ctas_per_sm(desc)
+    assert got_sms == sms and 1 <= per_sm <= 32
     mb = tables.shape[1]
     need = pkv.pkv_decode_workspace_bytes(desc, len(lens), mb)
-    assert need == pkv.pkv_decode_split_geometry(desc, len(lens), mb, sms)[2] > 0
+    assert need == pkv.pkv_decode_split_geometry(desc, len(lens), mb, sms, per_sm)[2] > 0
     k_t, v_t, q_t = to_torch(kp, "bf16"), to_torch(vp, "bf16"), to_torch(q, "bf16")
     t_t = torch.from_numpy(np.ascontiguousarray(tables)).cuda()
     l_t = torch.from_numpy(lens).cuda()
@@ -324,3 +327,37 @@ def test_pools_on_the_host_are_refused_before_launch():
     assert rc == pkv.PKV_ERR_INVALID_ARG
     assert pkv.pkv_launch_count() == before
     assert pkv.pkv_get_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_one_wave_long_partitions(dtype):
+    """Few sequences with long contexts take the one-wave split: partitions far longer than 64
+    blocks, whose table entries the kernel streams in chunks of 32 per warp (several chunks per
+    warp here). Against the oracle, also with a block id out of range deep inside a partition."""
+    n_q, n_kv, d = 8, 8, 64
+    probe = pkv.make_desc(dtype, 1, 1000, n_q, n_kv, d)
+    per_sm, sms = pkv.pkv_decode_ctas_per_sm(probe)
+    parts = sms * per_sm // (5 * n_kv)                  # 5 sequences x 8 KV heads = 40 pairs
+    top = 16 * 130 * parts                              # partitions of ~130 blocks: 5 chunks per warp
+    lens = [top, top // 2 + 3, 1, top - 5, 17]
+    q, kp, vp, tables, lens, nb = paged_case(dtype, lens, n_q, n_kv, d, seed=91)
+    desc = pkv.make_desc(dtype, 1, nb, n_q, n_kv, d)
+    bpp, n_parts, _ = pkv.pkv_decode_split_geometry(desc, len(lens), tables.shape[1], sms, per_sm)
+    assert bpp > 4 * 32 and n_parts == parts
+    scale = 1.0 / np.sqrt(d)
+    got, flags = run_decode(dtype, q, kp, vp, tables, lens, scale, n_q, n_kv, d)
+    want = oracle.paged_decode(dtype, q, kp[0], vp[0], tables, lens, scale)
+    assert flags == 0 and np.all(np.isfinite(got))
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
+    # a bad table entry deep inside a partition is skipped (its rows masked) and flagged
+    bad = tables.copy()
+    bad[0, 300] = nb + 5
+    got_bad, flags = run_decode(dtype, q, kp, vp, bad, lens, scale, n_q, n_kv, d)
+    assert flags & pkv.PKV_DEV_BAD_BLOCK_ID
+    # attention is a sum over the set of visible keys: dropping the full block 300 (16 keys) equals
+    # the same sequence without that table entry and 16 positions shorter (the tail block unchanged)
+    t0 = np.delete(tables[:1], 300, axis=1)
+    want0 = oracle.paged_decode(dtype, q[:1], kp[0], vp[0], t0, np.array([lens[0] - 16], np.int32), scale)
+    assert np.all(np.isfinite(got_bad))
+    assert np.max(np.abs(got_bad[:1] - want0)) <= TOL[dtype]
+    assert np.max(np.abs(got_bad[1:] - want[1:])) <= TOL[dtype]   # other sequences unaffected

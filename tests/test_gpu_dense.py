@@ -86,8 +86,8 @@ def test_dense_single_partition_and_overlap_flag_bit_identical():
     desc = pkv.make_desc("f16", 1, 1, 8, 8, 128)
     q_t, k_t, v_t = to_torch(q, "f16"), to_torch(kd, "f16"), to_torch(vd, "f16")
     l_t = torch.from_numpy(lens).cuda()
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    single = pkv.pkv_decode_split_geometry(desc, 80, 8, sms)[1] == 1
+    per_sm, sms = pkv.pkv_decode_ctas_per_sm(desc)
+    single = pkv.pkv_decode_split_geometry(desc, 80, 8, sms, per_sm)[1] == 1
     ws = pkv.alloc_workspace(desc, 80, 8)
     assert single == (ws is None)
     a = torch.empty_like(q_t)

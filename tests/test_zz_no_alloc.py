@@ -55,14 +55,16 @@ def test_static_scratch_matches_workspace_version_twice(dtype, n_q, n_kv, n_kv2,
 
 def test_static_scratch_rejects_oversized_calls_before_launching():
     desc, q, kp, vp, tables, lens = _inputs("f16", [40, 70], 4, 4, 64, seed=33)
-    big = 1 << 20                       # a table this wide would need far more than 16 MiB of partials
-    need = pkv.pkv_decode_workspace_bytes(desc, 2, big)
+    # 4,096 sequences (more (sequence, KV head) pairs than any GPU holds CTAs) with tables 2^20 blocks
+    # wide would need far more than 16 MiB of partials; the call is refused before anything is read
+    n_seqs, big = 4096, 1 << 20
+    need = pkv.pkv_decode_workspace_bytes(desc, n_seqs, big)
     assert need > 16 << 20
     before = pkv.pkv_launch_count()
     L = pkv.lib()
     rc = L.pkv_paged_decode_attention_static(
         ctypes.byref(desc), 0, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(kp.data_ptr()),
         ctypes.c_void_p(vp.data_ptr()), ctypes.c_void_p(tables.data_ptr()), big, ctypes.c_void_p(lens.data_ptr()),
-        2, ctypes.c_float(0.1), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(0))
+        n_seqs, ctypes.c_float(0.1), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(0))
     assert rc == pkv.PKV_ERR_UNSUPPORTED
     assert pkv.pkv_launch_count() == before
