@@ -157,7 +157,7 @@ inline int launch_status(cudaError_t err) {
 }
 
 // Cached TMA tensor map of one pool layer seen as rows x head_dim 16-bit elements (tmap.cu).
-enum { PKV_BOX_PANEL = 0, PKV_BOX_BLOCK = 1 };
+enum { PKV_BOX_PANEL = 0, PKV_BOX_BLOCK = 1, PKV_BOX_BLOCK_HALF = 2 };
 cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, int box, CUtensorMap* out);
 
 // Shared with decode_static.cu (abi.cu owns both): the current device's status word, and the

@@ -8,7 +8,9 @@ cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, c
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;  // TMA row coordinates are 32-bit
     CUtensorMap tk, tv;
     cudaError_t err = kv_tensor_map(a.k_layer, rows, head_dim, PKV_BF16, PKV_BOX_PANEL, &tk);
-    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, PKV_BOX_BLOCK, &tv);
+    // head_dim 256 runs as CTA pairs, each CTA copying half of every V block's columns
+    const int vbox = UmmaTuning<256>::PAIR && head_dim == 256 ? PKV_BOX_BLOCK_HALF : PKV_BOX_BLOCK;
+    if (err == cudaSuccess) err = kv_tensor_map(a.v_layer, rows, head_dim, PKV_BF16, vbox, &tv);
     if (err != cudaSuccess) return err;
     return launch_prefill_umma_dtype<__nv_bfloat16>(head_dim, group, a, tk, tv, stream);
 }

@@ -33,6 +33,10 @@
 //              waits on its own barriers.
 // S_{j+1} runs on the tensor pipe while the softmax warps work on S_j (they read S_j into registers
 // first and release its buffer).
+// At head_dim 256 two CTAs (a cluster of two adjacent query tiles) compute as one pair with
+// .cta_group::2 instructions (M = 256 rows, 128 per CTA): each CTA loads half of every K tile and
+// half of every V block, the even CTA issues the products, and the two exchange barrier arrivals
+// (see the kernel's comment); the roles of the warps are otherwise the same.
 // O is rescaled (read, multiplied, written back in TMEM) only when a row's running maximum grows
 // by more than 8 (a factor 2^8 in the weights): P <= 2^8 stays exact enough in the storage type
 // and the final division by the same running sum keeps the result the softmax's. The weights are
@@ -63,13 +67,14 @@ __device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// 3-D tensor copy of one whole (block, KV head) chunk: box 64 columns x 16 rows x D/64 panels,
-// landing as [panel][16 rows][128 B] (tensor map of the PKV_BOX_BLOCK kind).
-__device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const void* tmap, int row, uint64_t* bar) {
+// 3-D tensor copy of the panels pan0 .. of one (block, KV head) chunk: box 64 columns x 16 rows x
+// the map's panel count (all D/64 panels, or half of them for a CTA pair), landing as
+// [panel][16 rows][128 B] (tensor maps of the PKV_BOX_BLOCK / PKV_BOX_BLOCK_HALF kinds).
+__device__ __forceinline__ void tma_load_3d_keep(uint32_t dst, const void* tmap, int row, int pan0, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar))
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(pan0), "r"(smem_addr(bar))
         : "memory");
 }
 
@@ -135,14 +140,21 @@ struct UmmaTuning {
     // Keys per tile: 128, so that S = Q K^T runs as N = 128 instructions (one issuing thread cannot
     // keep up with N = 64 instructions).
     static constexpr int BN = 128;
+    // head_dim 256: CTA pairs. Alone, a CTA's shared memory carries ~320 KiB per 128-key tile (TMA
+    // writes of K and V, tensor-core reads of K, V and P, the softmax's writes of P): ~2,560 cycles
+    // at 128 B/cycle against 2,048 cycles of tensor work. Paired (a cluster of two CTAs holding
+    // adjacent query tiles of one sequence and KV head, .cta_group::2 instructions with M = 256),
+    // each CTA holds half of every K tile (64 of its 128 keys) and half of every V block (128 of
+    // the 256 columns): ~192 KiB per tile per SM, and half the L2 -> SM traffic.
+    static constexpr bool PAIR = D == 256;
     static constexpr bool PT = D <= 128;          // P in TMEM (A operand of PV) rather than shared memory
     static constexpr int SB = D == 256 ? 1 : 2;    // S buffers in TMEM
-    static constexpr int STK = D == 256 ? 2 : (D == 128 ? 3 : 4);  // K stages
+    static constexpr int STK = D == 256 ? 3 : (D == 128 ? 3 : 4);  // K stages
     // V stages hold VB 16-key blocks each, block-major ([block][panel][16 rows][128 B], one 3-D TMA
-    // copy per block). At d = 256 shared memory has room for 64 KiB of V next to two K stages and P:
-    // two half-tile stages, so V of tile j+1 streams in while PV_j still reads the other half.
+    // copy per block): half-tile stages at d = 256, so V of tile j+1 streams in while PV_j still
+    // reads the other half.
     static constexpr int VB = D == 256 ? 4 : 8;
-    static constexpr int STV = D == 256 ? 2 : (D == 128 ? 3 : 4);  // V stages
+    static constexpr int STV = D == 256 ? 4 : (D == 128 ? 3 : 4);  // V stages
     static constexpr int NP = D == 64 ? 2 : 1;     // P buffers
     // TMEM columns: S [0, SB*BN), O [SB*BN, +D), Q [.., +D/2), P [.., +NP*BN/2) when PT (16-bit
     // operands hold two elements per 32-bit column)
@@ -156,8 +168,10 @@ template <int D>
 struct UmmaSmem {
     using Tu = UmmaTuning<D>;
     static constexpr int BN = Tu::BN;
-    static constexpr size_t KT = (size_t)BN * D * 2;    // K tile [D/64][BN keys][128 B]
-    static constexpr size_t VT = (size_t)Tu::VB * 16 * D * 2;  // V stage [VB][D/64][16 keys][128 B]
+    static constexpr int KH = Tu::PAIR ? BN / 2 : BN;   // keys of each K tile this CTA holds
+    static constexpr int DH = Tu::PAIR ? D / 2 : D;     // V columns this CTA holds
+    static constexpr size_t KT = (size_t)KH * D * 2;    // K tile [D/64][KH keys][128 B]
+    static constexpr size_t VT = (size_t)Tu::VB * 16 * DH * 2;  // V stage [VB][DH/64][16 keys][128 B]
     static constexpr size_t PB = Tu::PT ? 0 : (size_t)128 * BN * 2;  // P [BN/64][128 rows][128 B]
     static constexpr size_t K = 0;                       // [STK] K tiles
     static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V stages
@@ -173,6 +187,25 @@ struct UmmaSmem {
     static constexpr size_t ALLOC = TOTAL + 1024;
 };
 
+// Paired CTAs (head_dim 256) split the work of one 256-row product as follows; the even CTA of the
+// cluster ("lead") issues every tcgen05.mma, the odd one ("peer") supplies half of the operands
+// and reads its half of the results from its own tensor memory:
+//   - both load their half of each K tile / V stage with their own tensor copies onto their own
+//     full_k / full_v barrier; the peer's warp 5 (K) and warp 7 (V) forward each completed phase
+//     to the lead's barrier, which therefore counts two arrivals (its own expect_tx and the peer's);
+//   - the peer's softmax threads arrive on the lead's q_ready, s_free and p_full barriers and its V
+//     producer on the lead's vtail (each count doubled);
+//   - the lead's MMA completions (commits onto its own s_full / k_empty and p_free / v_empty) are
+//     forwarded to the peer's barriers of the same name by the thread that issued them, once they
+//     have completed: S_{j+1} cannot start before both CTAs have read S_j (one S buffer), nor
+//     PV_{j+1} before both have rewritten P (one P buffer), so the issuer would wait there anyway.
+//     (A completion signal sent to both CTAs by the commit itself measured the same: the paired
+//     kernel runs at the part's power limit.)
+// A forwarded phase cannot be overtaken by the next one: every next phase of these barriers needs
+// an arrival that depends on the forwarded one. Every wait is bounded, and a CTA that gives up
+// still meets the other at the cluster barrier before it leaves. Remote arrivals carry the
+// instruction's default (CTA-scope) semantics: a cluster-scope release put microseconds on every
+// hand-off.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(256, 1)
     paged_prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_k,
@@ -181,22 +214,27 @@ __global__ void __launch_bounds__(256, 1)
     using Tu = UmmaTuning<D>;
     using S = UmmaSmem<D>;
     using M = MmaType<T>;
+    constexpr bool PAIR = Tu::PAIR;
+    constexpr int CG = PAIR ? 2 : 1;
     constexpr int BN = Tu::BN, SB = Tu::SB, STK = Tu::STK, STV = Tu::STV, NP = Tu::NP;
     constexpr int BPT = BN / kBlock;                    // blocks per tile
+    constexpr int KB = S::KH / kBlock;                  // blocks of each K tile this CTA loads
     constexpr int ROWS = 128;
     constexpr int QT = ROWS / G;
-    constexpr int PANELS = D / 64;
+    constexpr int PANELS = D / 64;                      // panels of a K block
+    constexpr int VPAN = S::DH / 64;                    // panels of a V block in this CTA
     constexpr uint32_t KT = (uint32_t)S::KT;
     constexpr uint32_t VT = (uint32_t)S::VT;
-    constexpr uint32_t PANEL = BN * 128;                // one 64-column panel of a K tile
-    constexpr uint32_t BLKB = kBlock * D * 2;           // one block of one KV head (a V stage holds VB)
+    constexpr uint32_t PANEL = S::KH * 128;             // one 64-column panel of this CTA's K tile
+    constexpr uint32_t KBLKB = kBlock * D * 2;          // one K block (all panels)
+    constexpr uint32_t BLKB = kBlock * S::DH * 2;       // this CTA's part of one V block
     constexpr int VB = Tu::VB;
     constexpr int VPT = BPT / VB;                       // V stages per tile
     static_assert(BPT % VB == 0, "whole V stages per tile");
     static_assert(Tu::PT ? VPT == 1 : (VB * kBlock) % 64 == 0, "a P part is whole 64-key panels");
     constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
-    constexpr uint32_t IDESC_S = umma_idesc_f16(BF, 128, BN, false);
-    constexpr uint32_t IDESC_PV = umma_idesc_f16(BF, 128, D, true);
+    constexpr uint32_t IDESC_S = umma_idesc_f16(BF, PAIR ? 256 : 128, BN, false);
+    constexpr uint32_t IDESC_PV = umma_idesc_f16(BF, PAIR ? 256 : 128, D, true);
     constexpr uint32_t S_COL = Tu::S_COL, O_COL = Tu::O_COL, Q_COL = Tu::Q_COL;
     static_assert(BPT <= 32, "one lane per block of a tile");
 
@@ -222,6 +260,8 @@ __global__ void __launch_bounds__(256, 1)
     // the same chunk) may start once every CTA has passed here and fill the SMs this grid's last
     // wave leaves idle. Without such a launch this is a no-op.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool lead = rank == 0;
     const int tile = a.q_tiles - 1 - (int)blockIdx.x;  // tiles with the most keys start first
     const int g = blockIdx.y;
     const int s = blockIdx.z;
@@ -239,70 +279,91 @@ __global__ void __launch_bounds__(256, 1)
         if (bad || qt < 0 || tq0 >= n_new) return 0;
         return (ctx - n_new + min(tq0 + QT, n_new) - 1) / BN + 1;
     };
-    const int n_tiles = key_tiles(tile);
-    if (n_tiles == 0) return;
+    // A pair walks the key tiles of its heavier query tile: both CTAs take part in every product
+    // (the lighter tile's causal mask zeroes the keys it does not see). Both compute the same count.
+    int n_tiles = key_tiles(tile);
+    if constexpr (PAIR) n_tiles = max(n_tiles, key_tiles(a.q_tiles - 1 - (int)(blockIdx.x ^ 1u)));
+    if (n_tiles == 0) return;  // both CTAs of a pair leave here together, before any cluster barrier
     const int t0 = tile * QT;
     const int pos0 = ctx - n_new + t0;
     const int nb = (ctx + kBlock - 1) / kBlock;
     const bool tail_tile = n_tiles * BN > ctx;  // the last tile holds rows past the context
 
     if (threadIdx.x == 0) {
-        // a stage is free again when the MMAs that read it are done with it (one commit)
+        // the lead's barriers that the peer also arrives on count both CTAs' arrivals
+        const uint32_t two = PAIR && lead ? 2u : 1u;
         for (int i = 0; i < STK; ++i) {
-            mbar_init(&full_k[i], 1);
+            mbar_init(&full_k[i], two);
             mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < STV; ++i) {
-            mbar_init(&full_v[i], 1);
+            mbar_init(&full_v[i], two);
             mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 128);
+            mbar_init(&s_free[i], 128 * two);
         }
         for (int i = 0; i < S::NPP; ++i) {
-            mbar_init(&p_full[i], 128);
+            mbar_init(&p_full[i], 128 * two);
             mbar_init(&p_free[i], 1);
         }
-        mbar_init(vtail, 32);
-        mbar_init(q_ready, 128);
+        mbar_init(vtail, 32 * two);
+        mbar_init(q_ready, 128 * two);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(taddr_s, Tu::TMEM_COLS);
+    if (warp == 5) tmem_alloc_cg<CG>(taddr_s, Tu::TMEM_COLS);
     tcgen05_before_sync();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers and tensor memory exist from here on
     tcgen05_after_sync();
     const uint32_t tmem = *taddr_s;
+    // an arrival on the lead's copy of one of this CTA's barriers (the peer's softmax threads and V
+    // producer: one remote operation per warp that counts its lanes), or on this CTA's own when it is
+    // the lead or works alone
+    auto arrive_lead = [&](uint64_t* bar) {
+        if (PAIR && !lead)
+            mbar_arrive_remote_warp(cluster_addr(bar, 0u));
+        else
+            mbar_arrive(bar);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool { return mbar_wait_bounded(bar, parity); };
 
     if (warp == 4 || warp == 6) {
         // ===================== producers: warp 4 moves K tiles, warp 6 moves V stages =====================
         // A K stage (one tile) is released once S_j has been computed, a V stage (VB blocks) once the
         // PV instructions that read it have: the next K tile lands while the softmax of this one runs.
-        // Unit u: K tile u (BPT blocks, panel-major, one 2-D copy per block and panel), or V stage u
-        // (VB blocks of tile u / VPT, block-major, one 3-D copy per block).
+        // Unit u: K tile u (its KB blocks of this CTA, panel-major, one 2-D copy per block and panel),
+        // or V stage u (VB blocks of tile u / VPT, block-major, one 3-D copy per block of this CTA's
+        // columns).
         const bool is_v = warp == 6;
         const int nst = is_v ? STV : STK;
         const int upt = is_v ? VPT : 1;           // units per tile
-        const int nbu = is_v ? VB : BPT;          // blocks per unit
+        const int nbu = is_v ? VB : KB;           // blocks per unit this CTA loads
         const int n_units = n_tiles * upt;
         uint64_t* full = is_v ? full_v : full_k;
         uint64_t* empty = is_v ? v_empty : k_empty;
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         const uint32_t ring = (uint32_t)(is_v ? S::V : S::K);
         const uint32_t ust = is_v ? VT : KT;      // bytes per stage
+        const uint32_t ubb = is_v ? BLKB : KBLKB; // bytes per block this CTA copies
+        // first block of unit u this CTA loads: V stages tile the block list; a pair splits each
+        // K tile's blocks between its CTAs (the lead the first KB)
+        auto unit_block0 = [&](int u) -> int { return is_v ? u * VB : u * BPT + (int)rank * KB; };
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
         int issued = 0;
         // lane l < nbu handles block l of every unit; its table entry is read one unit ahead, so
         // that the load's latency overlaps the wait for a free stage
-        int phys_next = lane < nbu && lane < nb ? __ldg(trow + lane) : -1;
+        int phys_next = lane < nbu && unit_block0(0) + lane < nb ? __ldg(trow + unit_block0(0) + lane) : -1;
         for (int u = 0; u < n_units; ++u) {
             const int j = u / upt;
             const int st = u % nst;
-            const int blk = u * nbu + lane;      // units tile the block list in order
+            const int blk = unit_block0(u) + lane;
             const bool inb = lane < nbu && blk < nb;
             const int phys = phys_next;
-            phys_next = lane < nbu && blk + nbu < nb ? __ldg(trow + blk + nbu) : -1;
-            if (u >= nst && !mbar_wait_bounded(&empty[st], (uint32_t)((u / nst) - 1) & 1u)) {
+            const int nblk = unit_block0(u + 1) + lane;
+            phys_next = lane < nbu && nblk < nb ? __ldg(trow + nblk) : -1;
+            if (u >= nst && !wait(&empty[st], (uint32_t)((u / nst) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
                 break;
             }
@@ -323,12 +384,14 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 __syncwarp();
             }
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(okm) * BLKB);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(okm) * ubb);
             __syncwarp();
             if (ok) {
                 const int row0 = (phys * a.n_kv + g) * kBlock;
                 if (is_v) {
-                    tma_load_3d_keep(sbase + ring + (uint32_t)st * VT + (uint32_t)lane * BLKB, tm, row0, &full[st]);
+                    // this CTA's VPAN panels of the block: panels rank * VPAN .. of the row
+                    tma_load_3d_keep(sbase + ring + (uint32_t)st * VT + (uint32_t)lane * BLKB, tm, row0,
+                                     (int)rank * VPAN, &full[st]);
                 } else {
                     const uint32_t dst = sbase + ring + (uint32_t)st * KT + (uint32_t)lane * 2048;
 #pragma unroll
@@ -344,18 +407,34 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 const int r0 = ctx - j * BN;               // 1 .. BN-1
                 const int lo = max(r0 - (u % VPT) * VB * kBlock, 0);  // first stage row to zero
-                for (int i = lane; i < (VB * kBlock - lo) * PANELS * 8; i += 32) {
-                    const int r = lo + i / (PANELS * 8);   // stage row = 16 x block + token
-                    const int pn = (i / 8) % PANELS;
+                for (int i = lane; i < (VB * kBlock - lo) * VPAN * 8; i += 32) {
+                    const int r = lo + i / (VPAN * 8);    // stage row = 16 x block + token
+                    const int pn = (i / 8) % VPAN;
                     reinterpret_cast<uint4*>(unit_ptr + (size_t)(r / kBlock) * BLKB + (size_t)pn * 2048 +
                                              (size_t)(r % kBlock) * 128)[i % 8] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                if (u == n_units - 1) mbar_arrive(vtail);
+                if (u == n_units - 1) arrive_lead(vtail);
             }
         }
         for (int u = max(0, issued - nst); u < issued; ++u)  // the copies of the last stages have landed
             mbar_wait_bounded(&full[u % nst], (uint32_t)(u / nst) & 1u);
+    } else if (PAIR && !lead && (warp == 5 || warp == 7)) {
+        // ===================== peer: forward this CTA's landed K tiles (warp 5) and V stages (warp 7) =====================
+        if (lane == 0) {
+            const bool is_v = warp == 7;
+            const int nst = is_v ? STV : STK;
+            const int n_units = n_tiles * (is_v ? VPT : 1);
+            uint64_t* full = is_v ? full_v : full_k;
+            for (int u = 0; u < n_units; ++u) {
+                if (!mbar_wait_bounded(&full[u % nst], (uint32_t)(u / nst) & 1u)) {
+                    atomicOr(a.status, (unsigned)PKV_DEV_WAIT_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_remote(cluster_addr(&full[u % nst], 0u));
+            }
+        }
+        __syncwarp();
     } else if (warp == 5 || warp == 7) {
         // ===================== MMA issuers: warp 5 S = Q K^T, warp 7 O += P V =====================
         // Two issuing threads: a tcgen05.mma takes ~50 cycles to issue from one thread and an
@@ -367,12 +446,12 @@ __global__ void __launch_bounds__(256, 1)
             bool ok = true;
             if (warp == 5) {
                 const uint64_t kdesc0 = umma_desc_sw128(sbase + (uint32_t)S::K, 16, 1024);
-                ok = mbar_wait_bounded(q_ready, 0u);
+                ok = wait(q_ready, 0u);
                 for (int j = 0; ok && j < n_tiles; ++j) {
                     const int st = j % STK;
                     const int b = j % SB;
-                    if (!mbar_wait_bounded(&full_k[st], (uint32_t)(j / STK) & 1u) ||
-                        (j >= SB && !mbar_wait_bounded(&s_free[b], (uint32_t)((j / SB) - 1) & 1u))) {
+                    if (!wait(&full_k[st], (uint32_t)(j / STK) & 1u) ||
+                        (j >= SB && !wait(&s_free[b], (uint32_t)((j / SB) - 1) & 1u))) {
                         ok = false;
                         break;
                     }
@@ -381,11 +460,21 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t d_s = tmem + S_COL + (uint32_t)(b * BN);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
-                        umma_f16_tmem_a(d_s, tmem + Q_COL + (uint32_t)ks * 8,
-                                        kd + (uint64_t)(((uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32) >> 4),
-                                        IDESC_S, ks > 0);
-                    umma_commit(&s_full[b]);
-                    umma_commit(&k_empty[st]);  // the K stage may take tile j + STK once S_j is done
+                        umma_f16_tmem_a_cg<CG>(d_s, tmem + Q_COL + (uint32_t)ks * 8,
+                                               kd + (uint64_t)(((uint32_t)(ks >> 2) * PANEL + (uint32_t)(ks & 3) * 32) >> 4),
+                                               IDESC_S, ks > 0);
+                    umma_commit_cg<CG>(&s_full[b]);
+                    umma_commit_cg<CG>(&k_empty[st]);  // the K stage may take tile j + STK once S_j is done
+                    if constexpr (PAIR) {
+                        // S_j done: the peer may read its rows of S_j and refill its half of the K stage
+                        if (!mbar_wait_bounded(&s_full[b], (uint32_t)(j / SB) & 1u) ||
+                            !mbar_wait_bounded(&k_empty[st], (uint32_t)(j / STK) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(cluster_addr(&s_full[b], 1u));
+                        mbar_arrive_remote(cluster_addr(&k_empty[st], 1u));
+                    }
                 }
             } else {
                 // V stage: block kk of the tile at + (kk % VB) * BLKB, its panels 2 KiB apart (leading
@@ -394,7 +483,7 @@ __global__ void __launch_bounds__(256, 1)
                 const uint64_t pdesc0 = umma_desc_sw128(sbase + (uint32_t)S::P, 16, 1024);
                 for (int j = 0; ok && j < n_tiles; ++j) {
                     const int pb = j % NP;
-                    if (j == n_tiles - 1 && tail_tile && !mbar_wait_bounded(vtail, 0u)) {
+                    if (j == n_tiles - 1 && tail_tile && !wait(vtail, 0u)) {
                         ok = false;
                         break;
                     }
@@ -403,8 +492,8 @@ __global__ void __launch_bounds__(256, 1)
                         // part h of P_j (the keys of V stage u) and the V stage itself
                         const int u = j * VPT + h;
                         const int sv = u % STV;
-                        if (!mbar_wait_bounded(&p_full[pb * VPT + h], (uint32_t)(j / NP) & 1u) ||
-                            !mbar_wait_bounded(&full_v[sv], (uint32_t)(u / STV) & 1u)) {
+                        if (!wait(&p_full[pb * VPT + h], (uint32_t)(j / NP) & 1u) ||
+                            !wait(&full_v[sv], (uint32_t)(u / STV) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -415,17 +504,32 @@ __global__ void __launch_bounds__(256, 1)
                             const int kk = h * VB + i;
                             const uint64_t bd = vd + (uint64_t)(((uint32_t)i * BLKB) >> 4);
                             if constexpr (Tu::PT) {
-                                umma_f16_tmem_a(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8), bd,
-                                                IDESC_PV, j > 0 || kk > 0);
+                                umma_f16_tmem_a_cg<CG>(tmem + O_COL, tmem + Tu::P_COL + (uint32_t)(pb * (BN / 2) + kk * 8),
+                                                       bd, IDESC_PV, j > 0 || kk > 0);
                             } else {
                                 const uint64_t ad = pdesc0 + (uint64_t)(((uint32_t)pb * (uint32_t)S::PB +
                                                                          (uint32_t)(kk >> 2) * (128 * 128) +
                                                                          (uint32_t)(kk & 3) * 32) >> 4);
-                                umma_f16(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
+                                umma_f16_cg<CG>(tmem + O_COL, ad, bd, IDESC_PV, j > 0 || kk > 0);
                             }
                         }
-                        umma_commit(&p_free[pb * VPT + h]);  // part h of P buffer pb may take P_{j+NP}
-                        umma_commit(&v_empty[sv]);           // the V stage may take unit u + STV
+                        umma_commit_cg<CG>(&p_free[pb * VPT + h]);  // part h of P buffer pb may take P_{j+NP}
+                        umma_commit_cg<CG>(&v_empty[sv]);           // the V stage may take unit u + STV
+                    }
+                    if constexpr (PAIR) {
+                        // PV_j done part by part: the peer may rewrite that part of its P and refill
+                        // its half of the V stage
+#pragma unroll
+                        for (int h = 0; ok && h < VPT; ++h) {
+                            const int u = j * VPT + h;
+                            if (!mbar_wait_bounded(&p_free[pb * VPT + h], (uint32_t)(j / NP) & 1u) ||
+                                !mbar_wait_bounded(&v_empty[u % STV], (uint32_t)(u / STV) & 1u)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_remote(cluster_addr(&p_free[pb * VPT + h], 1u));
+                            mbar_arrive_remote(cluster_addr(&v_empty[u % STV], 1u));
+                        }
                     }
                 }
             }
@@ -465,7 +569,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             tmem_wait_st();
             tcgen05_before_sync();
-            mbar_arrive(q_ready);
+            arrive_lead(q_ready);
         }
         float m_used = -INFINITY;
         float l = 0.f;
@@ -489,7 +593,7 @@ __global__ void __launch_bounds__(256, 1)
             const int pb = j % NP;
             const unsigned okm = okm_next;
             if (j + 1 < n_tiles) okm_next = tile_mask(j + 1);
-            if (!mbar_wait_bounded(&s_full[b], (uint32_t)(j / SB) & 1u)) {
+            if (!wait(&s_full[b], (uint32_t)(j / SB) & 1u)) {
                 ok = false;
                 break;
             }
@@ -500,7 +604,7 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld32(tmem + lane_base + S_COL + (uint32_t)(b * BN + c0), *reinterpret_cast<uint32_t(*)[32]>(&sc[c0]));
             tmem_wait_ld();
             tcgen05_before_sync();
-            mbar_arrive(&s_free[b]);  // the S buffer may take S_{j+SB}
+            arrive_lead(&s_free[b]);  // the S buffer may take S_{j+SB}
             const int key0 = j * BN;
             const bool unmasked = key0 + BN - 1 <= lim && okm == FULL;
             if (!unmasked) {
@@ -523,7 +627,7 @@ __global__ void __launch_bounds__(256, 1)
             const float alpha = grow ? exp2f(m_used - m_new) : 1.f;  // 0 when m_used is -inf
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // O holds P_0..P_{j-1} V: wait for the last PV, then scale this warp's 32 rows in TMEM
-                if (!mbar_wait_bounded(&p_free[((j - 1) % NP) * VPT + VPT - 1], (uint32_t)((j - 1) / NP) & 1u)) {
+                if (!wait(&p_free[((j - 1) % NP) * VPT + VPT - 1], (uint32_t)((j - 1) / NP) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -552,7 +656,7 @@ __global__ void __launch_bounds__(256, 1)
             // part h of P buffer pb is free once the instructions of PV_{j-NP} that read it are done
 #pragma unroll
             for (int h = 0; h < VPT; ++h) {
-                if (j >= NP && !mbar_wait_bounded(&p_free[pb * VPT + h], (uint32_t)((j / NP) - 1) & 1u)) {
+                if (j >= NP && !wait(&p_free[pb * VPT + h], (uint32_t)((j / NP) - 1) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -576,13 +680,13 @@ __global__ void __launch_bounds__(256, 1)
                     fence_proxy_async_smem();
                 }
                 tcgen05_before_sync();
-                mbar_arrive(&p_full[pb * VPT + h]);
+                arrive_lead(&p_full[pb * VPT + h]);
             }
             if (!ok) break;
         }
         if (ok) {
             const int last = n_tiles - 1;
-            if (!mbar_wait_bounded(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u)) ok = false;
+            if (!wait(&p_free[(last % NP) * VPT + VPT - 1], (uint32_t)(last / NP) & 1u)) ok = false;
         }
         // launched as a programmatic dependent, this grid computed while the previous kernel was
         // finishing; the outputs are written only once that kernel has completed (so a chain of
@@ -614,15 +718,19 @@ __global__ void __launch_bounds__(256, 1)
     }
     tcgen05_before_sync();
     __syncthreads();
+    // no CTA of a pair leaves (or releases its tensor memory) while the other may still arrive on
+    // its barriers or the pair's products may still write its tensor memory
+    if constexpr (PAIR) cluster_sync_all();
     if (warp == 5) {
         tcgen05_after_sync();
-        tmem_dealloc(tmem, Tu::TMEM_COLS);
+        tmem_dealloc_cg<CG>(tmem, Tu::TMEM_COLS);
     }
 }
 
 template <typename T, int D, int G>
 cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                     cudaStream_t stream) {
+    using Tu = UmmaTuning<D>;
     constexpr size_t smem = UmmaSmem<D>::ALLOC;
     static_assert(smem <= 227 * 1024, "shared memory per CTA");
     auto kern = paged_prefill_umma_kernel<T, D, G>;
@@ -635,17 +743,31 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
+    constexpr int CL = Tu::PAIR ? 2 : 1;
+    PrefillArgs b = a;
+    b.q_tiles = (a.q_tiles + CL - 1) / CL * CL;  // whole pairs; an extra query tile has no rows
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.q_tiles, a.n_kv, a.n_seqs);
+    cfg.gridDim = dim3(b.q_tiles, b.n_kv, b.n_seqs);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n_attr = 0;
+    if (CL > 1) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = CL;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    if (a.overlap_previous) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = a.overlap_previous ? 1 : 0;
-    err = cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
+    cfg.numAttrs = n_attr;
+    err = cudaLaunchKernelEx(&cfg, kern, b, tk, tv);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

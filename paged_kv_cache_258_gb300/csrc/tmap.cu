@@ -7,7 +7,9 @@
 //                  of several blocks must sit in one [panel][rows] array);
 //   PKV_BOX_BLOCK  3-D (64 columns, rows, D/64 panels at a 128-byte stride), a 64 x 16 x D/64 box:
 //                  the whole chunk in one copy, landing as [panel][16 rows][128 B] (the V tiles
-//                  of prefill, read by the tensor cores one 16-key block at a time).
+//                  of prefill, read by the tensor cores one 16-key block at a time);
+//   PKV_BOX_BLOCK_HALF  the same with a 64 x 16 x D/128 box: half of the chunk's columns (the V
+//                  blocks of a prefill CTA pair, whose CTAs each hold half of every V block).
 // Encoding goes through the driver entry point cuTensorMapEncodeTiled, found once through the
 // runtime; maps are cached by (address, shape, type, box, device) in a hash table so steady-state
 // calls do not re-encode: a step touches up to 3 maps per layer (K panels, V panels, V blocks), so
@@ -77,7 +79,8 @@ cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, int dtype, int box,
                           CUtensorMap* out) {
     if (dtype != PKV_F16 && dtype != PKV_BF16) return cudaErrorInvalidValue;
-    if (box != PKV_BOX_PANEL && box != PKV_BOX_BLOCK) return cudaErrorInvalidValue;
+    if (box != PKV_BOX_PANEL && box != PKV_BOX_BLOCK && box != PKV_BOX_BLOCK_HALF) return cudaErrorInvalidValue;
+    if (box == PKV_BOX_BLOCK_HALF && (head_dim % 128) != 0) return cudaErrorInvalidValue;
     if (rows <= 0 || rows >= (1LL << 31) || (head_dim % 64) != 0) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -101,13 +104,14 @@ cudaError_t kv_tensor_map(const void* layer_base, long long rows, int head_dim, 
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     err = encoder(&encode);
     if (err != cudaSuccess) return err;
-    const bool blk = box == PKV_BOX_BLOCK;
+    const bool blk = box != PKV_BOX_PANEL;
     const cuuint32_t rank = blk ? 3 : 2;
     // dims / box innermost first; strides (bytes) of dims 1.. (the panel dim of the 3-D form steps
     // 64 elements = 128 bytes inside a row)
     const cuuint64_t dims[3] = {blk ? 64u : (cuuint64_t)head_dim, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128};
-    const cuuint32_t boxdim[3] = {64, (cuuint32_t)kBlock, (cuuint32_t)(head_dim / 64)};
+    const cuuint32_t boxdim[3] = {64, (cuuint32_t)kBlock,
+                                  (cuuint32_t)(box == PKV_BOX_BLOCK_HALF ? head_dim / 128 : head_dim / 64)};
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     CUtensorMap map;
     CUresult r = encode(&map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,

@@ -206,8 +206,9 @@ def test_host_argument_errors():
 @pytest.mark.parametrize("trial", range(12))
 def test_random_batches_stress(trial):
     """Random mixes of sequences, chunk lengths, contexts and GQA groups (query tiles with no rows,
-    ragged last key tiles and chunks shorter than a tile appear throughout). Every output against
-    the oracle; the status word must stay clean (no bounded wait may give up)."""
+    ragged last key tiles and chunks shorter than a tile appear throughout; at head_dim 256 CTA
+    pairs, one of whose query tiles may have no rows or fewer keys than the other). Every output
+    against the oracle; the status word must stay clean (no bounded wait may give up)."""
     rng = np.random.default_rng(1000 + trial)
     dtype = ["bf16", "f16"][trial % 2]
     d = [256, 256, 128, 64][trial % 4]
@@ -227,7 +228,8 @@ def test_random_batches_stress(trial):
 
 @pytest.mark.parametrize("d,group", [(256, 4), (128, 1)])
 def test_cuda_graph_replay_of_prefill(d, group):
-    """A captured prefill launch replays bit-identically to the eager call, several times."""
+    """A captured prefill launch (CTA pairs at head_dim 256) replays bit-identically to the eager
+    call, several times."""
     import torch
     dtype, n_kv = "bf16", 2
     n_q = n_kv * group
