@@ -258,3 +258,29 @@ def test_cuda_graph_replay_of_prefill(d, group):
     assert pkv.pkv_get_device_status() == 0
     want = oracle.paged_prefill(dtype, q, kp[0], vp[0], tables, lens, qs, scale, n_threads=THREADS)
     assert np.max(np.abs(as_f64(out) - want)) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_pair_skips_bad_blocks_in_either_half(dtype):
+    """head_dim 256 runs as CTA pairs, each CTA loading half of every 128-key tile (blocks 0-3 the
+    even CTA, 4-7 the odd one) and half of every V block's columns. Out-of-range table entries in
+    both halves are skipped, their keys masked, and flagged. Attention is a sum over the set of
+    visible keys, so a query at position p equals a decode over the sequence with the skipped blocks
+    removed and |{0..p} minus the skipped positions| keys (which stay a prefix in that order)."""
+    n_q, n_kv, d = 8, 2, 256
+    c, n = 700, 300                                          # chunk at positions 400 .. 699
+    q, kp, vp, tables, lens, qs = prefill_case(dtype, [c], [n], n_q, n_kv, d, seed=23)
+    skipped = [30, 33]                                       # tile 3 block 6 (odd CTA), tile 4 block 1 (even)
+    bad = tables.copy()
+    for i, b in enumerate(skipped):
+        bad[0, b] = kp.shape[1] + 5 + i
+    scale = 1.0 / np.sqrt(d)
+    got, flags = run_prefill(dtype, q, kp, vp, bad, lens, qs, scale, n_q, n_kv, d)
+    assert flags & pkv.PKV_DEV_BAD_BLOCK_ID
+    assert np.all(np.isfinite(got))
+    reduced = np.delete(tables[0], skipped)
+    pos = np.arange(c - n, c)
+    visible = pos + 1 - sum(np.clip(pos + 1 - 16 * b, 0, 16) for b in skipped)
+    t_rep = np.ascontiguousarray(np.broadcast_to(reduced, (n, reduced.shape[0])))
+    want = oracle.paged_decode(dtype, q, kp[0], vp[0], t_rep, visible.astype(np.int32), scale)
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
