@@ -38,19 +38,24 @@ def test_fullsize_sampled(config, layers, seqs):
     mo = BlockManagerOracle(wl.num_blocks, free_order=W.free_order(wl.num_blocks, wl.seed))
     for s, n in enumerate(wl.context_lens):
         assert mo.add_seq(s, int(n) - 1)[0] == "ok"
+    # the batch's rows are its sequences longest first (bench.py orders fixed batches so); row r of
+    # q, the tables and out is sequence ids[r], and the appends go in row order
+    ids = [int(x) for x in batch.seq_ids]
+    assert sorted(ids) == list(range(wl.n_seqs))
+    assert all(wl.context_lens[a] >= wl.context_lens[b] for a, b in zip(ids, ids[1:]))
     n_steps = 4
     for _ in range(n_steps):
         st = batch.step(q, kn, vn, out, wl.scale)
-        slots = [mo.append_slot(s)[1] for s in range(wl.n_seqs)]
+        slots = [mo.append_slot(s)[1] for s in ids]
         assert st["slots"].numpy().tolist() == slots
         for l in layers:
             oracle.kv_append(to_host(kn[l], dtype), to_host(vn[l], dtype), np.array(slots), host_k[l], host_v[l])
     assert pkv.pkv_get_device_status() == 0
     tables = np.full((wl.n_seqs, batch.max_blocks), -1, dtype=np.int32)
     lens = np.zeros(wl.n_seqs, dtype=np.int32)
-    for s in range(wl.n_seqs):
-        t, lens[s] = mo.block_table(s)
-        tables[s, : len(t)] = t
+    for r, s in enumerate(ids):
+        t, lens[r] = mo.block_table(s)
+        tables[r, : len(t)] = t
     assert np.array_equal(tables, st["tables"].numpy()) and np.array_equal(lens, st["lens"].numpy())
     got = as_f64(out)
     sel = np.array(seqs)
