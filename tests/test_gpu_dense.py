@@ -120,3 +120,38 @@ def test_dense_rejects_bad_lengths_before_launch():
                                       vp(q.data_ptr()), vp(0), 0, 2, vp(0))  # unknown flag bit
     assert rc == pkv.PKV_ERR_INVALID_ARG
     assert pkv.pkv_launch_count() == before
+
+
+def test_dense_fullsize_gpt_layer_sampled():
+    """The dense comparison at the GPT-style batch's full size (64 sequences x 32 heads x 128 fp16,
+    lengths of the bench's workload, one layer), as bench.py times it: sampled sequences against
+    the oracle on their rows laid out as a pool with identity tables."""
+    import torch
+    wl = W.gpt(seed=W.BASE_SEED + 1)
+    L, B, n_kv, d = 1, wl.n_seqs, wl.n_kv_heads, wl.head_dim
+    lens = wl.context_lens.astype(np.int32)
+    s_max = int(-(-int(lens.max()) // 16) * 16)
+    desc = pkv.make_desc("f16", L, 1, wl.n_q_heads, n_kv, d)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    shape = pkv.dense_cache_shape(desc, B, s_max)
+    kc = torch.randn(shape, dtype=torch.float16, device="cuda", generator=g)
+    vc = torch.randn(shape, dtype=torch.float16, device="cuda", generator=g)
+    for s in range(B):                                   # rows past each context: never read
+        kc[:, s, :, int(lens[s]):] = float("nan")
+        vc[:, s, :, int(lens[s]):] = float("nan")
+    q = torch.randn((B, wl.n_q_heads, d), dtype=torch.float16, device="cuda", generator=g)
+    out = torch.full_like(q, float("nan"))
+    l_t = torch.from_numpy(lens).cuda()
+    ws = pkv.alloc_workspace(desc, B, s_max // 16)
+    pkv.pkv_dense_decode_attention(desc, 0, q, kc, vc, l_t, wl.scale, out, ws)
+    assert pkv.pkv_get_device_status() == 0
+    assert torch.isfinite(out.float()).all()
+    sel = [0, 9, 31, int(np.argmax(lens)), 63]
+    for s in sel:
+        kd = kc[:, s:s + 1].cpu().numpy()
+        vd = vc[:, s:s + 1].cpu().numpy()
+        tables = np.arange(s_max // 16, dtype=np.int32).reshape(1, -1)
+        want = oracle.paged_decode("f16", q[s:s + 1].cpu().numpy(), as_pool(kd)[0], as_pool(vd)[0], tables,
+                                   lens[s:s + 1], wl.scale)
+        assert np.max(np.abs(as_f64(out[s:s + 1]) - want)) <= TOL["f16"], s
