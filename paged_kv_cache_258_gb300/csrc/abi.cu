@@ -451,6 +451,24 @@ int pkv_paged_prefill_attention_ex(const pkv_cache_desc* d, int32_t layer, const
                         query_start, n_seqs, n_tokens, max_query_len, scale, out, stream);
 }
 
+int pkv_prefill_wave_tokens(const pkv_cache_desc* d, int32_t* tokens) {
+    int rc = pkv_validate_desc(d);
+    if (rc != PKV_OK) return rc;
+    if (!tokens) return PKV_ERR_INVALID_ARG;
+    int sms = 0, per_sm = 0;
+    const int group = d->n_q_heads / d->n_kv_heads;
+    if (pkv::current_sm_count(&sms) != cudaSuccess ||
+        pkv::prefill_ctas_per_sm(d->dtype, d->head_dim, group, &per_sm) != cudaSuccess || per_sm <= 0) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    // a CTA holds the rows of prefill_tokens_per_cta tokens of one KV head
+    const long long t = (long long)sms * per_sm * pkv::prefill_tokens_per_cta(d->dtype, d->head_dim, group) /
+                        d->n_kv_heads;
+    *tokens = (int32_t)(t > 0 ? t : 1);
+    return PKV_OK;
+}
+
 int pkv_copy_blocks(const pkv_cache_desc* d, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n_pairs,
                     void* stream) {
     int rc = pkv_validate_desc(d);

@@ -772,6 +772,32 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
     return cudaGetLastError();
 }
 
+// CTAs of the tensor-core prefill kernel one SM holds at once (shared and tensor memory, registers).
+template <typename T, int D, int G>
+cudaError_t prefill_umma_ctas_per_sm_tpl(int* out) {
+    constexpr size_t smem = UmmaSmem<D>::ALLOC;
+    auto kern = paged_prefill_umma_kernel<T, D, G>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, 256, smem);
+    if (err != cudaSuccess) return err;
+    // tensor memory: a CTA allocates TMEM_COLS of the SM's 512 columns for its whole life
+    const int by_tmem = 512 / (int)UmmaTuning<D>::TMEM_COLS;
+    if (*out > by_tmem) *out = by_tmem;
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t prefill_umma_ctas_per_sm_dtype(int head_dim, int group, int* out) {
+#define PKV_CASE(DD, GG) \
+    if (head_dim == DD && group == GG) return prefill_umma_ctas_per_sm_tpl<T, DD, GG>(out);
+    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+    PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+    PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
+#undef PKV_CASE
+    return cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t launch_prefill_umma_dtype(int head_dim, int group, const PrefillArgs& a, const CUtensorMap& tk,
                                       const CUtensorMap& tv, cudaStream_t stream) {

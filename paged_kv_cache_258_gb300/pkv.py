@@ -72,6 +72,7 @@ def lib():
         "pkv_decode_split_geometry": (ctypes.c_int, [dp, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_i32),
                                                      ctypes.POINTER(c_i32), ctypes.POINTER(c_sz)]),
         "pkv_decode_ctas_per_sm": (ctypes.c_int, [dp, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]),
+        "pkv_prefill_wave_tokens": (ctypes.c_int, [dp, ctypes.POINTER(c_i32)]),
         "pkv_kv_append": (ctypes.c_int, [dp, c_i32, vp, vp, vp, c_i32, vp, vp, vp]),
         "pkv_paged_decode_attention": (ctypes.c_int, [dp, c_i32, vp, vp, vp, vp, c_i32, vp, c_i32, ctypes.c_float,
                                                       vp, vp, c_sz, vp]),
@@ -216,6 +217,19 @@ def pkv_decode_split_geometry(desc: CacheDesc, n_seqs: int, max_blocks_per_seq: 
                                            ctypes.byref(nbytes)),
            "pkv_decode_split_geometry")
     return int(bpp.value), int(nparts.value), int(nbytes.value)
+
+
+def pkv_prefill_wave_tokens(desc: CacheDesc) -> int:
+    """Tokens of one sequence's chunk that fill one wave of the prefill grid on the current device."""
+    t = ctypes.c_int32(0)
+    _check(lib().pkv_prefill_wave_tokens(ctypes.byref(desc), ctypes.byref(t)), "pkv_prefill_wave_tokens")
+    return int(t.value)
+
+
+def wave_aligned_chunk(desc: CacheDesc, target: int) -> int:
+    """The whole number of prefill waves (at least one) closest to `target` tokens per chunk."""
+    w = pkv_prefill_wave_tokens(desc)
+    return w * max(1, int(round(target / w)))
 
 
 def pkv_decode_ctas_per_sm(desc: CacheDesc):

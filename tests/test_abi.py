@@ -187,3 +187,13 @@ def test_launchers_refuse_host_tensors_before_any_cuda_call():
         pkv.prefill_launcher(desc, q, pool, pool, tables, lens, torch.zeros(4, dtype=torch.int32), 1, 0.1, q)
     with pytest.raises(ValueError):
         pkv.append_launcher(desc, k, k, torch.zeros(3, dtype=torch.int64), pool, pool)
+
+
+def test_wave_aligned_chunk_rounds_to_whole_waves(monkeypatch):
+    """The chunk helper keeps a whole number (at least one) of prefill waves, the one closest to the
+    target: 2,048 tokens over waves of 1,216 -> 2,432; over waves of 3,000 -> one wave."""
+    d = pkv.make_desc("bf16", 1, 64, 16, 4, 256)
+    for wave, target, want in [(1216, 2048, 2432), (1216, 1000, 1216), (3000, 2048, 3000), (512, 2048, 2048),
+                               (600, 2048, 1800)]:
+        monkeypatch.setattr(pkv, "pkv_prefill_wave_tokens", lambda desc, w=wave: w)
+        assert pkv.wave_aligned_chunk(d, target) == want, (wave, target)

@@ -284,3 +284,21 @@ def test_pair_skips_bad_blocks_in_either_half(dtype):
     t_rep = np.ascontiguousarray(np.broadcast_to(reduced, (n, reduced.shape[0])))
     want = oracle.paged_decode(dtype, q, kp[0], vp[0], t_rep, visible.astype(np.int32), scale)
     assert np.max(np.abs(got - want)) <= TOL[dtype]
+
+
+def test_prefill_wave_tokens_fill_whole_waves():
+    """pkv_prefill_wave_tokens: the chunk tokens of one sequence that fill exactly one wave of the
+    prefill grid (SMs x CTAs per SM x tokens per CTA / KV heads); at head_dim 256 one CTA holds an SM
+    (its shared and tensor memory), so the wave is one CTA per SM."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    d256 = pkv.make_desc("bf16", 16, 4096, 16, 4, 256)
+    w = pkv.pkv_prefill_wave_tokens(d256)
+    assert w == sms * (128 // 4) // 4
+    assert pkv.wave_aligned_chunk(d256, 2048) == w * max(1, round(2048 / w))
+    for dtype, n_q, n_kv, d in [("f16", 32, 32, 128), ("bf16", 8, 8, 64), ("f32", 4, 2, 64)]:
+        desc = pkv.make_desc(dtype, 1, 1024, n_q, n_kv, d)
+        w = pkv.pkv_prefill_wave_tokens(desc)
+        per_cta = (32 if dtype == "f32" else 128) // (n_q // n_kv)
+        ctas = w * n_kv // per_cta
+        assert w >= 1 and ctas % sms == 0 and ctas // sms >= 1, (dtype, d, w)
