@@ -698,6 +698,12 @@ def run_prefill_gpu(args) -> dict | None:
     total_flops = reduce_over_ranks(flops, "sum", device)
     attn_ms = sum(a.elapsed_time(b) for a, b in ev)
     achieved = flops / (attn_ms * 1e-3) / 1e12
+    # algorithmic bytes of a launch: its chunk's q rows read and output rows written, and the K/V rows
+    # of every visible key read once (keys 0 .. c0 + n - 1 of the prompt)
+    row_q, row_kv = n_q * d * 2, n_kv * d * 2
+    alg_bytes = sum(2 * n * row_q + 2 * (c0 + n) * row_kv for c0, n in chunks) / len(chunks)
+    traffic = traffic_per_launch("prefill30k", alg_bytes, "paged_prefill_prefill30k.traffic.json",
+                                 PREFILL_SOURCES)
 
     # e2e: every chunk's q / new K / new V rows (all layers) from pinned host memory and its outputs
     # back, on copy streams beside the kernels. Each chunk has its own rows in the device buffers, so
@@ -783,7 +789,10 @@ def run_prefill_gpu(args) -> dict | None:
         "prompt_tokens_per_s": round(prompt * args.steps * ws / (ms * 1e-3), 1),
         "roofline": {"kernel": "paged_prefill_umma_kernel (tcgen05, S and O in tensor memory, TMA K/V producers)",
                      "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_note": "DRAM bytes per launch: a late chunk's ncu capture scaled by the mean "
+                                     "launch's algorithmic bytes",
+                     "algorithmic_bytes_per_launch": int(alg_bytes),
                      "launch_ms_mean": round(attn_ms / n_launch, 4),
                      "algorithmic_flops_per_launch": int(flops / n_launch)},
         "e2e": {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -877,6 +886,7 @@ def run_e2e(args, batch, cache, state, bufs, scale, device) -> dict:
 
 DECODE_SOURCES = ("decode.cuh", "decode_mma.cuh", "common.cuh")
 COPY_SOURCES = ("append_copy.cu", "common.cuh")
+PREFILL_SOURCES = ("prefill_umma.cuh", "umma.cuh", "decode_mma.cuh", "common.cuh", "prefill_bf16.cu")
 
 
 def traffic_per_launch(config: str, algorithmic: float, profile: str | None = None,
