@@ -176,13 +176,23 @@ struct UmmaSmem {
     static constexpr size_t K = 0;                       // [STK] K tiles
     static constexpr size_t V = K + (size_t)Tu::STK * KT;  // [STV] V stages
     static constexpr size_t P = V + (size_t)Tu::STV * VT;  // [NP] P tiles
-    static constexpr size_t BARS = P + (size_t)Tu::NP * PB;
+    // Q staging at the start, QC columns of all 128 rows per pass (16-byte units of a row XOR-swizzled
+    // by the row): the P buffer where P lives in shared memory (first written after every softmax
+    // thread has moved its row of Q into tensor memory), else a region of its own
+    static constexpr int QC = D < 128 ? D : 128;
+    static constexpr size_t QSB = (size_t)128 * QC * 2;
+    static constexpr bool Q_IN_P = Tu::NP * PB >= QSB;
+    static constexpr size_t QS = Q_IN_P ? P : P + (size_t)Tu::NP * PB;
+    static constexpr size_t BARS = Q_IN_P ? P + (size_t)Tu::NP * PB : QS + QSB;
     // full_k[STK] k_empty[STK] full_v[STV] v_empty[STV] s_full[SB] s_free[SB] p_full[NP * VPT]
     // p_free[NP * VPT] (one pair per part of a P buffer that one V stage's instructions read)
     // vtail q_ready
     static constexpr int NPP = Tu::NP * (Tu::BN / 16 / Tu::VB);
     static constexpr int NBARS = 2 * Tu::STK + 2 * Tu::STV + 2 * Tu::SB + 2 * NPP + 2;
     static constexpr size_t TADDR = BARS + (size_t)NBARS * 8;  // TMEM base address
+    // output staging at the end (in the K ring): 128 rows of D * 2 bytes, 16 bytes apart in banks
+    static constexpr size_t OROW = (size_t)D * 2 + 16;
+    static_assert(128 * OROW <= (size_t)Tu::STK * KT, "output rows fit in the K ring");
     static constexpr size_t TOTAL = TADDR + 16;
     static constexpr size_t ALLOC = TOTAL + 1024;
 };
@@ -288,6 +298,34 @@ __global__ void __launch_bounds__(256, 1)
     const int pos0 = ctx - n_new + t0;
     const int nb = (ctx + kBlock - 1) / kBlock;
     const bool tail_tile = n_tiles * BN > ctx;  // the last tile holds rows past the context
+    // The tile's query rows, loaded here by the softmax warps with every load in flight at once, so
+    // that their latency overlaps the barrier and tensor-memory setup below. Coalesced: a load
+    // instruction covers RPI rows' QC-column segments (LPR lanes of 16 bytes each per row), and the
+    // softmax role turns the warp's 32 rows around through shared memory so that thread t holds row t
+    // (TMEM lane t). (One row per thread straight from global memory cost each CTA ~2.5-4 us: every
+    // 16-byte load of a warp touched 32 rows.)
+    constexpr int QC = S::QC;
+    constexpr int QPASS = D / QC;        // passes of QC columns
+    constexpr int LPR = QC * 2 / 16;     // lanes per row segment (16 or 8)
+    constexpr int RPI = 32 / LPR;        // rows per load instruction
+    constexpr int QI = 32 / RPI;         // load instructions per pass
+    static_assert(LPR % 8 == 0 && LPR <= 16, "a row segment spans whole 128-byte bank sets");
+    uint4 qreg[QPASS * QI];
+    if (threadIdx.x < ROWS) {
+        const int l = threadIdx.x & 31;
+#pragma unroll
+        for (int i = 0; i < QI; ++i) {
+            const int r = (threadIdx.x & ~31) + i * RPI + l / LPR;  // query row of this load
+            const int tt = r / G;
+            const bool live = t0 + tt < n_new;
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.q) +
+                                                              ((size_t)(q0 + t0 + tt) * a.n_q + (size_t)g * G + r % G) * D) +
+                               l % LPR;
+#pragma unroll
+            for (int pass = 0; pass < QPASS; ++pass)
+                qreg[pass * QI + i] = live ? __ldg(src + pass * (QC / 8)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     if (threadIdx.x == 0) {
         // the lead's barriers that the peer also arrives on count both CTAs' arrivals
@@ -546,26 +584,39 @@ __global__ void __launch_bounds__(256, 1)
         // ===================== softmax (warps 0-3): thread = query row = TMEM lane =====================
         const int row = threadIdx.x;
         const int tt = row / G;
-        const bool live = t0 + tt < n_new;
         const int lim = min(pos0 + tt, ctx - 1);
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float sl = a.scale_log2;
         {
-            // this thread's query row -> TMEM lane `row` (the A operand of S = Q K^T); zero past the chunk
-            const uint4* qrow = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.q) +
-                                                               ((size_t)(q0 + t0 + tt) * a.n_q + (size_t)g * G + row % G) * D);
-#pragma unroll 1
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                uint32_t qv[32];
+            // this thread's query row -> TMEM lane `row` (the A operand of S = Q K^T; zero past the
+            // chunk): the warp's loaded segments go to its own 32 rows of the staging area, unit u of
+            // row rr at 16-byte position u ^ (rr & 7) (eight consecutive rows in distinct banks), and
+            // each thread reads its row back
+            unsigned char* qs = smem + S::QS + (size_t)warp * 32 * (QC * 2);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 w = live ? __ldg(qrow + c0 / 4 + c) : make_uint4(0u, 0u, 0u, 0u);
-                    qv[4 * c] = w.x;
-                    qv[4 * c + 1] = w.y;
-                    qv[4 * c + 2] = w.z;
-                    qv[4 * c + 3] = w.w;
+            for (int pass = 0; pass < QPASS; ++pass) {
+                if (pass > 0) __syncwarp();  // the previous pass has been read
+#pragma unroll
+                for (int i = 0; i < QI; ++i) {
+                    const int rr = i * RPI + lane / LPR;
+                    *reinterpret_cast<uint4*>(qs + (size_t)rr * (QC * 2) + (size_t)(((lane % LPR) ^ (rr & 7)) << 4)) =
+                        qreg[pass * QI + i];
                 }
-                tmem_st32(tmem + lane_base + Q_COL + (uint32_t)c0, qv);
+                __syncwarp();
+                uint32_t qv[QC / 2];
+#pragma unroll
+                for (int u = 0; u < LPR; ++u) {
+                    const uint4 x =
+                        *reinterpret_cast<const uint4*>(qs + (size_t)lane * (QC * 2) + (size_t)((u ^ (lane & 7)) << 4));
+                    qv[4 * u] = x.x;
+                    qv[4 * u + 1] = x.y;
+                    qv[4 * u + 2] = x.z;
+                    qv[4 * u + 3] = x.w;
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < QC / 2; c0 += 32)
+                    tmem_st32(tmem + lane_base + Q_COL + (uint32_t)(pass * (QC / 2) + c0),
+                              *reinterpret_cast<const uint32_t(*)[32]>(&qv[c0]));
             }
             tmem_wait_st();
             tcgen05_before_sync();
@@ -697,21 +748,42 @@ __global__ void __launch_bounds__(256, 1)
         } else {
             tcgen05_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            T* orow = reinterpret_cast<T*>(a.out) + ((size_t)(q0 + t0 + tt) * a.n_q + (size_t)g * G + row % G) * D;
+            // The rows go out through shared memory: written directly from the thread that owns a
+            // row, every 16-byte store of a warp hit 32 rows (~2.4 us per CTA at head_dim 256). The K
+            // ring is idle here: every K and V copy has landed and every product that read them has
+            // completed (the last PV, which this thread has just waited for, follows them all). A
+            // row stride of D * 2 + 16 bytes puts the 16-byte writes of eight consecutive rows in
+            // distinct banks.
+            unsigned char* srow = smem + S::K + (size_t)row * S::OROW;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(tmem + lane_base + O_COL + (uint32_t)c0, ov);
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t ov[64];
+                tmem_ld32(tmem + lane_base + O_COL + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+                tmem_ld32(tmem + lane_base + O_COL + (uint32_t)c0 + 32u, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
                 tmem_wait_ld();
-                uint32_t w[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    w[c] = M::pack(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
-                if (live) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(orow + c0 + 8 * c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2],
-                                                                                  w[4 * c + 3]);
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(srow + (size_t)c0 * 2 + 16 * c) =
+                        make_uint4(M::pack(__uint_as_float(ov[8 * c]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
+                                   M::pack(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
+                                   M::pack(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
+                                   M::pack(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
+            }
+            __syncwarp();
+            // then the warp's 32 rows leave UPR 16-byte units a row, RPS rows per store instruction
+            // (512 contiguous bytes at head_dim 256); rows past the chunk are not written
+            constexpr int UPR = D / 8;
+            constexpr int RPS = 32 / UPR;
+            const unsigned char* wrows = smem + S::K + (size_t)(warp * 32) * S::OROW;
+#pragma unroll 4
+            for (int k = 0; k < 32 / RPS; ++k) {
+                const int rr = k * RPS + lane / UPR;
+                const int r = warp * 32 + rr;
+                const int t = r / G;
+                if (t0 + t < n_new) {
+                    T* dst = reinterpret_cast<T*>(a.out) + ((size_t)(q0 + t0 + t) * a.n_q + (size_t)g * G + r % G) * D;
+                    reinterpret_cast<uint4*>(dst)[lane % UPR] =
+                        *reinterpret_cast<const uint4*>(wrows + (size_t)rr * S::OROW + (size_t)(lane % UPR) * 16);
                 }
             }
         }
