@@ -425,6 +425,14 @@ def measure_decode(args, config: str, device, rank: int, ws: int, read_peak: dic
         res["hbm_frac_of_read_peak"] = round(value / rp, 4)
         res["roofline"]["read_peak_gbs"] = rp
         res["roofline"]["frac_of_read_peak"] = round(achieved_gbs / rp, 4)
+    rf = res["roofline"]
+    if rf["traffic"] is not None:
+        # the same launches on the bytes DRAM actually moved (the shared-prefix workload reads its
+        # shared blocks from L2 after the first reader, so its logical GB/s exceeds any HBM figure)
+        rf["dram_gbs"] = round(rf["traffic"] / (rf["launch_ms_mean"] * 1e-3) / 1e9, 2)
+        rf["frac_on_dram_bytes"] = round(rf["dram_gbs"] / hbm_peak, 4)
+        if read_peak:
+            rf["frac_on_dram_bytes_of_read_peak"] = round(rf["dram_gbs"] / read_peak["best_gbs"], 4)
     if cpu:
         res["cpu_baseline"] = cpu_baseline(cache, batch, wl, budget_s=cpu_budget)
     del cache, batch, q, k_new, v_new, out, state
