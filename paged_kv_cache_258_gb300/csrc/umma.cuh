@@ -32,6 +32,7 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(bool bf16, int m, int n, b
 // CTAs on two SMs of a cluster computing one M = 256 product: each holds half of the rows of A and
 // D and half of the N columns of B, at the same shared-memory and tensor-memory offsets, and one
 // thread of the even CTA issues). A kernel uses one form throughout; CG selects it.
+// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 template <int CG>
 __device__ __forceinline__ void umma_f16_cg(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             bool accumulate) {
@@ -50,6 +51,8 @@ __device__ __forceinline__ void umma_f16_cg(uint32_t d_tmem, uint64_t a_desc, ui
     }
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A's row i in TMEM lane i, two 16-bit elements per 32-bit column
+// (a 16-element k-step is 8 columns).
 template <int CG>
 __device__ __forceinline__ void umma_f16_tmem_a_cg(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                                    bool accumulate) {
@@ -152,47 +155,6 @@ __device__ __forceinline__ void mbar_arrive_remote_warp(uint32_t cluster_bar) {
 // Every thread of every CTA of the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]: A's row i in TMEM lane i, two 16-bit elements per 32-bit column
-// (a 16-element k-step is 8 columns).
-__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-
-// The mbarrier gets one arrival when every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-                 : "memory");
-}
-
-// Whole-warp TMEM allocation of `ncols` columns (a power of two >= 32); the address lands in *dst.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tcgen05_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
