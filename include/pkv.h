@@ -188,7 +188,9 @@ int pkv_kv_append(const pkv_cache_desc* desc, int32_t layer, const void* k, cons
  *                 share one workspace.
  * Rows outside the valid positions (tails of last blocks, unreferenced blocks) are never
  * used: NaN there cannot reach the output. A table entry outside [0, num_blocks) is
- * skipped (its rows count as masked) and sets PKV_DEV_BAD_BLOCK_ID.
+ * skipped (its rows count as masked) and sets PKV_DEV_BAD_BLOCK_ID. fp16 / bf16 pools of
+ * 2^31 rows per layer or more (num_blocks * n_kv_heads * 16; the tensor copies' row
+ * coordinates are 32-bit) return PKV_ERR_UNSUPPORTED, launching nothing.
  */
 int pkv_paged_decode_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
                                const void* k_pool, const void* v_pool, const int32_t* block_tables,
@@ -324,6 +326,8 @@ int pkv_paged_decode_attention_static(const pkv_cache_desc* desc, int32_t layer,
  * them directly; the first fp16 / bf16 call on a pool layer checks this before building its copy
  * descriptors (cached afterwards by address) and returns PKV_ERR_INVALID_ARG for host memory or
  * another GPU's memory, launching nothing. The same holds for the fp16 / bf16 decode calls.
+ * fp16 / bf16 pools of 2^31 rows per layer or more (num_blocks * n_kv_heads * 16) return
+ * PKV_ERR_UNSUPPORTED, launching nothing (the tensor copies' row coordinates are 32-bit).
  */
 int pkv_paged_prefill_attention(const pkv_cache_desc* desc, int32_t layer, const void* q,
                                 const void* k_pool, const void* v_pool, const int32_t* block_tables,

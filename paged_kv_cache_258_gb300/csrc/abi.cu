@@ -312,6 +312,7 @@ static int decode_call(uint32_t flags, const pkv_cache_desc* d, int32_t layer, c
     // num_blocks = n_seqs * max_blocks
     const int num_blocks = dense ? n_seqs * max_blocks_per_seq : d->num_blocks;
     const long long rows = (long long)num_blocks * d->n_kv_heads * d->block_size;
+    if (d->dtype != PKV_F32 && rows >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;  // tensor-copy rows are 32-bit
     int bpp = 0, n_parts = 0;
     if (pkv::decode_geometry(d, rows, n_seqs, max_blocks_per_seq, &bpp, &n_parts) != cudaSuccess) return PKV_ERR_CUDA;
     size_t off_ml = 0, off_cnt = 0;

@@ -62,10 +62,11 @@ extern "C" int pkv_paged_decode_attention_static(const pkv_cache_desc* d, int32_
     if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
 
+    const long long rows = (long long)d->num_blocks * d->n_kv_heads * d->block_size;
+    if (d->dtype != PKV_F32 && rows >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;  // tensor-copy rows are 32-bit
     // Same partition geometry, hence the same scratch need, as pkv_paged_decode_attention.
     int bpp = 0, n_parts = 0;
-    if (pkv::decode_geometry(d, (long long)d->num_blocks * d->n_kv_heads * d->block_size, n_seqs, max_blocks_per_seq,
-                             &bpp, &n_parts) != cudaSuccess)
+    if (pkv::decode_geometry(d, rows, n_seqs, max_blocks_per_seq, &bpp, &n_parts) != cudaSuccess)
         return PKV_ERR_CUDA;
     size_t off_ml = 0, off_cnt = 0;
     const size_t need =

@@ -1,0 +1,138 @@
+"""The boundary's size limits on the GPU: the largest batch a launch takes (65,535 sequences, the
+grid's z extent) runs and matches the fp64 oracle, and one sequence more, or a table row longer
+than 2^24 entries, is refused with a status code before anything is launched.
+
+Unused pool rows are NaN-poisoned (vectorised here: the batches are too large for per-token loops).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import TOL, as_f64, to_torch
+from paged_kv_cache_258_gb300 import pkv
+from paged_kv_cache_258_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+MAX_SEQS = 65535
+
+
+def big_case(dtype, lens, n_q, n_kv, d, seed):
+    """Pools [1, num_blocks, n_kv, 16, d] with shuffled tables; every row that is not a valid row of
+    some sequence is NaN."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    nb = -(-lens.astype(np.int64) // W.BLOCK)
+    num_blocks = int(nb.sum()) + 3
+    tables = W.shuffled_tables(lens, num_blocks, seed)
+    kp = W.normal_values(rng, (1, num_blocks, n_kv, W.BLOCK, d), dtype)
+    vp = W.normal_values(rng, (1, num_blocks, n_kv, W.BLOCK, d), dtype)
+    # valid (block, offset) pairs: token j of sequence s is row j % 16 of block tables[s, j // 16]
+    seq = np.repeat(np.arange(len(lens)), lens)
+    j = np.arange(int(lens.sum())) - np.repeat(np.cumsum(lens) - lens, lens)
+    valid = np.zeros((num_blocks, W.BLOCK), dtype=bool)
+    valid[tables[seq, j // W.BLOCK], j % W.BLOCK] = True
+    nanv = W.nan_value(dtype)
+    for pool in (kp, vp):
+        pool[0].transpose(0, 2, 1, 3)[~valid] = nanv
+    return kp, vp, tables, lens, num_blocks
+
+
+def test_decode_largest_batch_matches_oracle():
+    import torch
+    dtype, n_q, n_kv, d = "f16", 2, 1, 64
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 40, size=MAX_SEQS)
+    kp, vp, tables, lens, num_blocks = big_case(dtype, lens, n_q, n_kv, d, seed=11)
+    q = W.normal_values(rng, (MAX_SEQS, n_q, d), dtype)
+    scale = 1.0 / np.sqrt(d)
+    desc = pkv.make_desc(dtype, 1, num_blocks, n_q, n_kv, d)
+    q_t = to_torch(q, dtype)
+    out = torch.full_like(q_t, float("nan"))
+    t_t = torch.from_numpy(np.ascontiguousarray(tables)).cuda()
+    l_t = torch.from_numpy(lens).cuda()
+    ws = pkv.alloc_workspace(desc, MAX_SEQS, tables.shape[1])
+    pkv.pkv_paged_decode_attention(desc, 0, q_t, to_torch(kp, dtype), to_torch(vp, dtype), t_t, l_t, scale, out, ws)
+    assert pkv.pkv_get_device_status() == 0
+    got = as_f64(out)
+    want = oracle.paged_decode(dtype, q, kp[0], vp[0], tables, lens, scale)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
+
+
+def test_prefill_largest_batch_matches_oracle():
+    import torch
+    dtype, n_q, n_kv, d = "f16", 4, 2, 64
+    rng = np.random.default_rng(12)
+    lens = rng.integers(1, 40, size=MAX_SEQS)
+    n_new = np.minimum(lens, rng.integers(1, 6, size=MAX_SEQS)).astype(np.int32)
+    kp, vp, tables, lens, num_blocks = big_case(dtype, lens, n_q, n_kv, d, seed=12)
+    qs = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    q = W.normal_values(rng, (int(qs[-1]), n_q, d), dtype)
+    scale = 1.0 / np.sqrt(d)
+    desc = pkv.make_desc(dtype, 1, num_blocks, n_q, n_kv, d)
+    q_t = to_torch(q, dtype)
+    out = torch.full_like(q_t, float("nan"))
+    pkv.pkv_paged_prefill_attention(
+        desc, 0, q_t, to_torch(kp, dtype), to_torch(vp, dtype), torch.from_numpy(np.ascontiguousarray(tables)).cuda(),
+        torch.from_numpy(lens).cuda(), torch.from_numpy(qs).cuda(), int(n_new.max()), scale, out)
+    assert pkv.pkv_get_device_status() == 0
+    got = as_f64(out)
+    want = oracle.paged_prefill(dtype, q, kp[0], vp[0], tables, lens, qs, scale)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
+
+
+def test_one_sequence_past_the_limit_is_refused():
+    """65,536 sequences: PKV_ERR_UNSUPPORTED from decode and prefill, nothing launched (every length
+    is 0 and every table entry block 0, so a launch, were one to happen, would read nothing)."""
+    import torch
+    n = MAX_SEQS + 1
+    desc = pkv.make_desc("f16", 1, 4, 2, 1, 64)
+    pool = torch.zeros(pkv.pool_shape(desc), dtype=torch.float16, device="cuda")
+    q = torch.zeros((n, 2, 64), dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    tables = torch.zeros((n, 1), dtype=torch.int32, device="cuda")
+    lens = torch.zeros((n,), dtype=torch.int32, device="cuda")
+    ws = torch.zeros((1 << 20,), dtype=torch.uint8, device="cuda")
+    before = pkv.pkv_launch_count()
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_decode_attention(desc, 0, q, pool, pool, tables, lens, 0.125, out, ws)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    qs = torch.arange(n + 1, dtype=torch.int32, device="cuda").clamp_(max=n)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_prefill_attention(desc, 0, q, pool, pool, tables, torch.ones_like(lens), qs, 1, 0.125, out)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    assert pkv.pkv_launch_count() == before
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_status() == 0
+
+
+def test_table_rows_past_2_24_entries_are_refused():
+    """max_blocks_per_seq above 2^24: PKV_ERR_INVALID_ARG from decode and prefill before any read of
+    the tables (the row claimed here is longer than the buffer behind it; the one sequence has
+    length 1, so a launch would read entry 0 only)."""
+    import torch
+    desc = pkv.make_desc("bf16", 1, 4, 2, 2, 64)
+    pool = torch.zeros(pkv.pool_shape(desc), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros_like(q)
+    tables = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    lens = torch.ones((1,), dtype=torch.int32, device="cuda")
+    qs = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    ws = torch.zeros((1 << 20,), dtype=torch.uint8, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    L = pkv.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    too_long = (1 << 24) + 1
+    before = pkv.pkv_launch_count()
+    rc = L.pkv_paged_decode_attention(ctypes.byref(desc), 0, p(q), p(pool), p(pool), p(tables), too_long, p(lens), 1,
+                                      ctypes.c_float(0.125), p(out), p(ws), ctypes.c_size_t(ws.numel()), stream)
+    assert rc == pkv.PKV_ERR_INVALID_ARG
+    rc = L.pkv_paged_prefill_attention(ctypes.byref(desc), 0, p(q), p(pool), p(pool), p(tables), too_long, p(lens),
+                                       p(qs), 1, 1, 1, ctypes.c_float(0.125), p(out), stream)
+    assert rc == pkv.PKV_ERR_INVALID_ARG
+    assert pkv.pkv_launch_count() == before
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_status() == 0

@@ -302,3 +302,37 @@ def test_prefill_wave_tokens_fill_whole_waves():
         per_cta = (32 if dtype == "f32" else 128) // (n_q // n_kv)
         ctas = w * n_kv // per_cta
         assert w >= 1 and ctas % sms == 0 and ctas // sms >= 1, (dtype, d, w)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_pools_past_32_bit_rows_are_refused(dtype):
+    """A layer of 2^31 rows or more (num_blocks x n_kv_heads x 16) cannot be addressed by the tensor
+    copies' 32-bit row coordinates: prefill and decode return PKV_ERR_UNSUPPORTED before launching.
+    The descriptor claims such a pool over small buffers; every other argument keeps a launch, were
+    one to happen, inside them (one sequence of one token in block 0)."""
+    import ctypes
+    import torch
+    n_kv, d = 2, 64
+    huge = pkv.make_desc(dtype, 1, (1 << 31) // (n_kv * 16), 2, n_kv, d)
+    dt = pkv.torch_dtype(dtype)
+    small = torch.zeros((1, 4, n_kv, 16, d), dtype=dt, device="cuda")
+    q = torch.zeros((1, 2, d), dtype=dt, device="cuda")
+    out = torch.zeros_like(q)
+    tables = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    lens = torch.ones((1,), dtype=torch.int32, device="cuda")
+    qs = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    ws = torch.zeros((1 << 20,), dtype=torch.uint8, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    L = pkv.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = L.pkv_paged_prefill_attention(ctypes.byref(huge), 0, p(q), p(small), p(small), p(tables), 1, p(lens),
+                                       p(qs), 1, 1, 1, ctypes.c_float(0.125), p(out), stream)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED
+    rc = L.pkv_paged_decode_attention(ctypes.byref(huge), 0, p(q), p(small), p(small), p(tables), 1, p(lens), 1,
+                                      ctypes.c_float(0.125), p(out), p(ws), ctypes.c_size_t(ws.numel()), stream)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED
+    rc = L.pkv_paged_decode_attention_static(ctypes.byref(huge), 0, p(q), p(small), p(small), p(tables), 1, p(lens),
+                                             1, ctypes.c_float(0.125), p(out), stream)
+    assert rc == pkv.PKV_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_status() == 0
