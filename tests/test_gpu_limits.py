@@ -85,8 +85,9 @@ def test_prefill_largest_batch_matches_oracle():
 
 
 def test_one_sequence_past_the_limit_is_refused():
-    """65,536 sequences: PKV_ERR_UNSUPPORTED from decode and prefill, nothing launched (every length
-    is 0 and every table entry block 0, so a launch, were one to happen, would read nothing)."""
+    """65,536 sequences: PKV_ERR_UNSUPPORTED from decode and prefill, nothing launched. (A launch
+    would need a grid z extent of 65,536, which CUDA rejects; its reads would stay in block 0: every
+    table entry is 0, decode lengths 0, prefill one token at position 0.)"""
     import torch
     n = MAX_SEQS + 1
     desc = pkv.make_desc("f16", 1, 4, 2, 1, 64)
@@ -136,3 +137,39 @@ def test_table_rows_past_2_24_entries_are_refused():
     assert pkv.pkv_launch_count() == before
     torch.cuda.synchronize()
     assert pkv.pkv_get_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_empty_batches_are_no_ops(dtype):
+    """Zero sequences, tokens or pairs: every device call returns PKV_OK, launches nothing and leaves
+    the pools and outputs as they were."""
+    import torch
+    desc = pkv.make_desc(dtype, 2, 8, 4, 2, 64)
+    dt = pkv.torch_dtype(dtype)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    kp = torch.randn(pkv.pool_shape(desc), device="cuda", generator=g).to(dt)
+    vp = torch.randn(pkv.pool_shape(desc), device="cuda", generator=g).to(dt)
+    k0, v0 = kp.clone(), vp.clone()
+    q = torch.zeros((0, 4, 64), dtype=dt, device="cuda")
+    out = torch.zeros((0, 4, 64), dtype=dt, device="cuda")
+    rows = torch.zeros((0, 2, 64), dtype=dt, device="cuda")
+    tables = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    lens = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    slots = torch.zeros((0,), dtype=torch.int64, device="cuda")
+    pairs = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    qs = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    dense = torch.zeros((2, 0, 2, 16, 64), dtype=dt, device="cuda")
+    before = pkv.pkv_launch_count()
+    pkv.pkv_kv_append(desc, 1, rows, rows, slots, kp, vp)
+    pkv.pkv_copy_blocks(desc, kp, vp, pairs)
+    pkv.pkv_paged_decode_attention(desc, 1, q, kp, vp, tables, lens, 0.125, out)
+    pkv.pkv_paged_decode_append_attention(desc, 1, q, rows, rows, kp, vp, tables, lens, 0.125, out)
+    pkv.pkv_paged_decode_attention_static(desc, 1, q, kp, vp, tables, lens, 0.125, out)
+    pkv.pkv_dense_decode_attention(desc, 1, q, dense, dense, lens, 0.125, out)
+    pkv.pkv_paged_prefill_attention(desc, 1, q, kp, vp, tables, lens, qs, 0, 0.125, out)
+    assert pkv.pkv_launch_count() == before
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_device_status() == 0
+    assert torch.equal(kp.view(torch.uint8), k0.view(torch.uint8))
+    assert torch.equal(vp.view(torch.uint8), v0.view(torch.uint8))
