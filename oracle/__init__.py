@@ -50,7 +50,10 @@ def build(force: bool = False) -> Path:
 def lib():
     global _lib
     if _lib is None:
-        path = build()
+        # PKV_ORACLE_LIB names another build of oracle.c to load instead (the mutation tests point
+        # it at copies with a planted mistake, to show that the pins reject them)
+        override = os.environ.get("PKV_ORACLE_LIB")
+        path = Path(override) if override else build()
         L = ctypes.CDLL(str(path))
         vp, i32p, i64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
         L.oracle_paged_decode.argtypes = [
