@@ -914,11 +914,16 @@ def traffic_per_launch(config: str, algorithmic: float, profile: str | None = No
 
 
 def kernel_source_hash(sources: tuple = DECODE_SOURCES) -> str:
+    """sha256 of the kernel sources' code: comments dropped and whitespace runs collapsed, so that a
+    documentation edit does not void counters taken on the same code (string literals are kept)."""
     import hashlib
+    import re
+    token = re.compile(r'("(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\')|//[^\n]*|/\*.*?\*/', re.S)
     h = hashlib.sha256()
     csrc = ROOT / "paged_kv_cache_258_gb300" / "csrc"
     for name in sources:
-        h.update((csrc / name).read_bytes())
+        code = token.sub(lambda m: m.group(1) or " ", (csrc / name).read_text())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()
 
 

@@ -14,10 +14,12 @@
 // issue one (an N = 64 instruction would leave the pipe waiting for its issuer). Eight warps:
 //   warps 0-3  softmax: thread t owns query row t, which is TMEM lane t (a warp reaches only its
 //              own 32 lanes). It first writes its row of Q into TMEM (the A operand of S = Q K^T:
-//              no shared-memory reads of Q per instruction), then per tile reads its row of S,
+//              no shared-memory reads of Q per instruction; the warp loads its 32 rows coalesced
+//              and turns them around through shared memory), then per tile reads its row of S,
 //              masks by selection, keeps the running max and sum in registers and writes its row
 //              of P (storage type) into TMEM (d <= 128) or shared memory (d = 256, where TMEM is
-//              full: S 128 + O 256 + Q 128 columns);
+//              full: S 128 + O 256 + Q 128 columns); at the end it scales its row of O by 1 / sum
+//              and the warp stores its rows coalesced, staged in the idle K ring;
 //   warps 4, 6 producers: walk the block table and move the K tiles (warp 4; a 2-D copy per block
 //              and 64-column panel, landing panel-major so that S = Q K^T reads 128 keys per
 //              instruction) and V stages of VB blocks (warp 6; one 3-D copy per block, landing

@@ -39,11 +39,16 @@ def test_traffic_scales_with_algorithmic_bytes(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     csrc = tmp_path / "paged_kv_cache_258_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for name in bench.PREFILL_SOURCES:
-        (csrc / name).write_text(f"// {name}\n")
+    for i, name in enumerate(bench.PREFILL_SOURCES):
+        (csrc / name).write_text(f"// {name}\nint v{i} = {i};  /* a value */\n")
     rec["kernel_source_sha256"] = bench.kernel_source_hash(bench.PREFILL_SOURCES)
     (tmp_path / "profiles" / "t.json").write_text(json.dumps(rec))
     got = bench.traffic_per_launch("x", 1.0e8, "t.json", bench.PREFILL_SOURCES)
     assert got == int(rec["dram_bytes_per_algorithmic_byte"] * 1.0e8)
-    (csrc / bench.PREFILL_SOURCES[0]).write_text("// changed\n")
+    # a comment or layout edit keeps the record; a code edit voids it
+    (csrc / bench.PREFILL_SOURCES[0]).write_text("// reworded\nint   v0 =\n 0; // a value\n")
+    assert bench.traffic_per_launch("x", 1.0e8, "t.json", bench.PREFILL_SOURCES) == got
+    (csrc / bench.PREFILL_SOURCES[0]).write_text("int v0 = 1;\n")
+    assert bench.traffic_per_launch("x", 1.0e8, "t.json", bench.PREFILL_SOURCES) is None
+    (csrc / bench.PREFILL_SOURCES[0]).write_text('int v0 = 0; const char* s = "// kept";\n')
     assert bench.traffic_per_launch("x", 1.0e8, "t.json", bench.PREFILL_SOURCES) is None
