@@ -357,7 +357,9 @@ int pkv_paged_prefill_attention_ex(const pkv_cache_desc* desc, int32_t layer, co
  * Scheduling helper for chunked prefill (the pages slice long prompts into chunks, "01 -
  * Conceito", paragraph 5, but fix no chunk size): *tokens receives how many new tokens of one
  * sequence fill exactly one wave of pkv_paged_prefill_attention's grid on the current device:
- * SMs x prefill CTAs one SM holds x tokens per CTA (128 / G query rows; 32 / G for fp32) / n_kv_heads.
+ * the CTAs the GPU holds at once (SMs x CTAs per SM; at head_dim 256, whose CTAs work in pairs, no
+ * more than twice the pairs the cluster scheduler can place at once) x tokens per CTA (128 / G query
+ * rows; 32 / G for fp32) / n_kv_heads.
  * A chunk of a whole number of waves leaves no SM idle through a partly filled last wave (head_dim
  * 256 on a GB300: 1,216 tokens; chunks of 2,432 run 12 % faster per launch than chunks of 2,048).
  * PKV_ERR_CUDA without a usable device; descriptor errors as pkv_validate_desc.

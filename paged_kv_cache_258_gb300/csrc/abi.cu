@@ -456,16 +456,15 @@ int pkv_prefill_wave_tokens(const pkv_cache_desc* d, int32_t* tokens) {
     int rc = pkv_validate_desc(d);
     if (rc != PKV_OK) return rc;
     if (!tokens) return PKV_ERR_INVALID_ARG;
-    int sms = 0, per_sm = 0;
+    int sms = 0, wave = 0;
     const int group = d->n_q_heads / d->n_kv_heads;
     if (pkv::current_sm_count(&sms) != cudaSuccess ||
-        pkv::prefill_ctas_per_sm(d->dtype, d->head_dim, group, &per_sm) != cudaSuccess || per_sm <= 0) {
+        pkv::prefill_wave_ctas(d->dtype, d->head_dim, group, sms, &wave) != cudaSuccess || wave <= 0) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
     // a CTA holds the rows of prefill_tokens_per_cta tokens of one KV head
-    const long long t = (long long)sms * per_sm * pkv::prefill_tokens_per_cta(d->dtype, d->head_dim, group) /
-                        d->n_kv_heads;
+    const long long t = (long long)wave * pkv::prefill_tokens_per_cta(d->dtype, d->head_dim, group) / d->n_kv_heads;
     *tokens = (int32_t)(t > 0 ? t : 1);
     return PKV_OK;
 }

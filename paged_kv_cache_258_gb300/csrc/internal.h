@@ -130,11 +130,12 @@ cudaError_t launch_prefill(int dtype, int head_dim, int group, const PrefillArgs
 cudaError_t launch_prefill_f32(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(int head_dim, int group, const PrefillArgs& a, cudaStream_t stream);
-// CTAs per SM of the prefill kernel of this shape on the current device (occupancy calculator,
-// tensor memory included).
-cudaError_t prefill_ctas_per_sm(int dtype, int head_dim, int group, int* out);
-cudaError_t prefill_ctas_per_sm_f16(int head_dim, int group, int* out);
-cudaError_t prefill_ctas_per_sm_bf16(int head_dim, int group, int* out);
+// CTAs of the prefill kernel of this shape that the current device (sms SMs) holds at once: the
+// occupancy calculator per SM, tensor memory included, and for CTA pairs the clusters the GPU can
+// place at once.
+cudaError_t prefill_wave_ctas(int dtype, int head_dim, int group, int sms, int* out);
+cudaError_t prefill_wave_ctas_f16(int head_dim, int group, int sms, int* out);
+cudaError_t prefill_wave_ctas_bf16(int head_dim, int group, int sms, int* out);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 // dst device, src device-visible page-locked host memory; both 16-byte aligned, bytes % 4 == 0.

@@ -15,8 +15,8 @@ cudaError_t launch_prefill_f16(int head_dim, int group, const PrefillArgs& a, cu
     return launch_prefill_umma_dtype<__half>(head_dim, group, a, tk, tv, stream);
 }
 
-cudaError_t prefill_ctas_per_sm_f16(int head_dim, int group, int* out) {
-    return prefill_umma_ctas_per_sm_dtype<__half>(head_dim, group, out);
+cudaError_t prefill_wave_ctas_f16(int head_dim, int group, int sms, int* out) {
+    return prefill_umma_wave_ctas_dtype<__half>(head_dim, group, sms, out);
 }
 
 }  // namespace pkv

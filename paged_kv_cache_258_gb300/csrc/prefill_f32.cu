@@ -139,17 +139,20 @@ cudaError_t launch_f32_tpl(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 template <int D, int G>
-cudaError_t f32_ctas_per_sm_tpl(int* out) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, paged_prefill_f32_kernel<D, G>, 256, 0);
+cudaError_t f32_wave_ctas_tpl(int sms, int* out) {
+    int per_sm = 0;
+    const cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_prefill_f32_kernel<D, G>, 256, 0);
+    *out = sms * per_sm;
+    return err;
 }
 
 }  // namespace
 
-cudaError_t prefill_ctas_per_sm(int dtype, int head_dim, int group, int* out) {
-    if (dtype == PKV_F16) return prefill_ctas_per_sm_f16(head_dim, group, out);
-    if (dtype == PKV_BF16) return prefill_ctas_per_sm_bf16(head_dim, group, out);
+cudaError_t prefill_wave_ctas(int dtype, int head_dim, int group, int sms, int* out) {
+    if (dtype == PKV_F16) return prefill_wave_ctas_f16(head_dim, group, sms, out);
+    if (dtype == PKV_BF16) return prefill_wave_ctas_bf16(head_dim, group, sms, out);
 #define PKV_CASE(DD, GG) \
-    if (head_dim == DD && group == GG) return f32_ctas_per_sm_tpl<DD, GG>(out);
+    if (head_dim == DD && group == GG) return f32_wave_ctas_tpl<DD, GG>(sms, out);
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
     PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)

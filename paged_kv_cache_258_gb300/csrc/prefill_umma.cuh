@@ -846,25 +846,46 @@ cudaError_t launch_prefill_umma_tpl(const PrefillArgs& a, const CUtensorMap& tk,
     return cudaGetLastError();
 }
 
-// CTAs of the tensor-core prefill kernel one SM holds at once (shared and tensor memory, registers).
+// CTAs of the tensor-core prefill kernel the GPU holds at once (one wave): SMs x CTAs per SM (shared
+// memory, registers, tensor memory), and for CTA pairs no more than the pairs the cluster scheduler
+// can place at once (an SM without a free partner in its GPC cannot hold half a pair).
 template <typename T, int D, int G>
-cudaError_t prefill_umma_ctas_per_sm_tpl(int* out) {
+cudaError_t prefill_umma_wave_ctas_tpl(int sms, int* out) {
     constexpr size_t smem = UmmaSmem<D>::ALLOC;
     auto kern = paged_prefill_umma_kernel<T, D, G>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, 256, smem);
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
     if (err != cudaSuccess) return err;
     // tensor memory: a CTA allocates TMEM_COLS of the SM's 512 columns for its whole life
     const int by_tmem = 512 / (int)UmmaTuning<D>::TMEM_COLS;
-    if (*out > by_tmem) *out = by_tmem;
+    if (per_sm > by_tmem) per_sm = by_tmem;
+    *out = sms * per_sm;
+    if constexpr (UmmaTuning<D>::PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (err != cudaSuccess) return err;
+        if (2 * clusters < *out) *out = 2 * clusters;
+    }
     return cudaSuccess;
 }
 
 template <typename T>
-cudaError_t prefill_umma_ctas_per_sm_dtype(int head_dim, int group, int* out) {
+cudaError_t prefill_umma_wave_ctas_dtype(int head_dim, int group, int sms, int* out) {
 #define PKV_CASE(DD, GG) \
-    if (head_dim == DD && group == GG) return prefill_umma_ctas_per_sm_tpl<T, DD, GG>(out);
+    if (head_dim == DD && group == GG) return prefill_umma_wave_ctas_tpl<T, DD, GG>(sms, out);
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
     PKV_CASE(256, 1) PKV_CASE(256, 2) PKV_CASE(256, 4) PKV_CASE(256, 8)
